@@ -1,0 +1,36 @@
+"""Mutation testing of the oracle's pins.
+
+Each build of the oracle with W4_ORACLE_MUTANT=n carries one planted mistake
+(the list is in oracle/w4_oracle.c, after the pitfalls table of "Fused int4
+and int8 dequantize-matmul in C", section 5).  A mutant is killed when at
+least one pin fails on it; every mutant must be killed.
+"""
+import pytest
+
+from tests import oracle_pins
+
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23]
+# pins too slow to repeat for every mutant, and not needed to kill any of them
+_SKIP = {"f16_bruteforce", "bf16"}
+
+
+@pytest.mark.parametrize("mutant", MUTANTS)
+def test_mutant_is_killed(mutant):
+    import oracle
+    o = oracle.get(mutant=mutant)
+    assert o.mutant == mutant
+    failed = []
+    for name, fn in sorted(oracle_pins.PINS.items()):
+        if name in _SKIP:
+            continue
+        try:
+            fn(o)
+        except AssertionError:
+            failed.append(name)
+    if mutant == 12:
+        # a partition that drops a row also shows up against the serial build
+        try:
+            oracle_pins.pool_equals_serial(oracle.get(), oracle.get(mutant=12, openmp=True))
+        except AssertionError:
+            failed.append("pool_equals_serial")
+    assert failed, f"mutant {mutant} survived every pin"
