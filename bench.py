@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Benchmark of the fused int4 dequantize-matmul on GB300.
+
+Default workload: group-wise W4A16 GEMV, M = 1, K = N = 2048, G = 32 (bf16 x,
+signed int4 W, f16 group scales) -- the decode step the int4 GEMV metric is
+quoted on.  A step is one linear over one batch (one activation row) with a
+weight matrix that is cold in L2: the timed loop rotates over enough weight
+copies to exceed twice the L2 size, so every step streams its weights from
+HBM.  Steps are replayed from CUDA graphs and timed with CUDA events.
+
+Metric: weight GB/s = (packed int4 bytes + f16 scale bytes) per step / time.
+Also reported: the roofline of the GEMV kernel against the measured HBM copy
+bandwidth, the oracle timed on the host cores (cpu_baseline), an end-to-end
+figure through the public API with host buffers, and extra lines for the
+other workloads (W4A8 GEMV, decode batch, microdecoder, prefill).
+
+--impl reference times the CPU oracle (plain C, row-parallel build) on the
+same workload and metric.  Multi-GPU runs (torchrun) are replicas: each rank
+runs the whole workload on its own GPU; there is no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FALLBACK = 129 * 1024 * 1024
+HBM_FALLBACK_GBS = 6800.0
+
+
+# ---------------------------------------------------------------- workloads
+
+WORKLOADS = {
+    "w4a16_gemv_m1": dict(kind="w4a16", M=1, N=2048, K=2048, G=32, layout=0,
+                          desc="group-wise W4A16 GEMV, M=1, K=N=2048, G=32, bf16 x, f16 scales"),
+    "w4a8_gemv_m1": dict(kind="w4a8", M=1, N=2048, K=2048, G=0, layout=0,
+                         desc="W4A8 linear_q4 GEMV, M=1, K=N=2048, per-channel Q4, per-row Q8 x"),
+    "w4a16_decode_m16_n13312": dict(kind="w4a16", M=16, N=13312, K=2048, G=128, layout=0,
+                                    desc="W4A16 decode batch M=16, K=2048, N=13312, G=128"),
+    "w4a16_decode_m1_n13312_il": dict(kind="w4a16", M=1, N=13312, K=2048, G=128, layout=1,
+                                      desc="W4A16 M=1, K=2048, N=13312, G=128, interleaved [N/64][K][32] layout"),
+    "w4a8_decode_m16_n13312": dict(kind="w4a8", M=16, N=13312, K=2048, G=0, layout=0,
+                                   desc="W4A8 decode batch M=16, K=2048, N=13312"),
+}
+
+
+def weight_bytes(w) -> int:
+    N, K, G = w["N"], w["K"], w["G"]
+    kp = K + (K & 1)
+    packed = N * (kp // 2)
+    scales = N * (kp // G) * 2 if w["kind"] == "w4a16" else N * 4
+    return packed + scales
+
+
+def step_bytes(w) -> int:
+    """Algorithmic bytes of one launch: weights + scales + activations + output."""
+    M, N, K = w["M"], w["N"], w["K"]
+    xb = M * K * (2 if w["kind"] == "w4a16" else 1) + (0 if w["kind"] == "w4a16" else 4 * M)
+    return weight_bytes(w) + xb + M * N * 4
+
+
+# ---------------------------------------------------------------- helpers
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": HBM_FALLBACK_GBS, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.lines = []
+        self.proc = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[4:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi gave no samples"}
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        note = None
+        if not inside:
+            # timed region shorter than the sampling period: nearest samples around it
+            inside = sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:3]
+            note = "timed region shorter than the 50 ms sampling period; nearest samples"
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for nm, v in zip(names[1:], r[4][1:]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        out = {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+               "reasons": sorted(reasons), "samples": len(inside)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_inputs(w, seed=1001):
+    from w4a16_int4_quantized_gb300 import synth
+    if w["kind"] == "w4a16":
+        return synth.w4a16_inputs(seed, w["M"], w["N"], w["K"], w["G"])
+    x, W = synth.w4a8_inputs(seed, w["M"], w["N"], w["K"])
+    return x, W
+
+
+def time_oracle(w, seconds: float, openmp: bool = True):
+    """Runs the oracle on a bounded sample: whole calls until `seconds` elapse."""
+    import oracle
+    o = oracle.get(openmp=openmp)
+    cores = os.cpu_count() if openmp else 1
+    if w["kind"] == "w4a16":
+        x, wp, s = oracle_inputs(w)
+        call = lambda: o.linear_w4a16_lanes(x, wp, s, w["K"], w["G"])
+        what = "ref_linear_w4a16_lanes"
+    else:
+        x, W = oracle_inputs(w)
+        xq, sx, _ = o.quantize_row_q8(x)
+        wp, sw = o.quantize_matrix_q4(W)
+        call = lambda: o.linear_q4(xq, sx, wp, sw, w["K"])
+        what = "ref_linear_q4"
+    call()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        call()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    gbs = n * weight_bytes(w) / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} full calls of {what} on {w['desc']} ({el:.1f} s)"}, n, el
+
+
+# ---------------------------------------------------------------- GPU measurement
+
+class Workload:
+    def __init__(self, w, copies: int):
+        import torch
+        from w4a16_int4_quantized_gb300 import ops, synth
+        self.w, self.ops = w, ops
+        M, N, K, G = w["M"], w["N"], w["K"], w["G"]
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.copies = copies
+        if w["kind"] == "w4a16":
+            x, wp, s = synth.w4a16_inputs(1001, M, N, K, G)
+            self.x = [dev(x) for _ in range(copies)]
+            w0 = dev(wp)
+            if w["layout"] == 1:
+                w0 = ops.pack_interleaved_n64(w0, K)
+            self.wt = [w0.clone() for _ in range(copies)]
+            self.s = [dev(s) for _ in range(copies)]
+        else:
+            x, W = synth.w4a8_inputs(1001, M, N, K)
+            xq, sx, _ = ops.quantize_row_q8(dev(x))
+            wq, sw = ops.quantize_matrix_q4(dev(W))
+            if w["layout"] == 1:
+                wq = ops.pack_interleaved_n64(wq, K)
+            self.x = [xq.clone() for _ in range(copies)]
+            self.sx = [sx.clone() for _ in range(copies)]
+            self.wt = [wq.clone() for _ in range(copies)]
+            self.s = [sw.clone() for _ in range(copies)]
+        self.y = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(copies)]
+        torch.cuda.synchronize()
+
+    def launch(self, i: int, flags: int = 1):
+        w, ops = self.w, self.ops
+        c = i % self.copies
+        if w["kind"] == "w4a16":
+            ops.linear_w4a16_group(self.x[c], self.wt[c], self.s[c], w["G"], K=w["K"], N=w["N"],
+                                   layout=w["layout"], flags=flags, out=self.y[c])
+        else:
+            ops.linear_q4(self.x[c], self.sx[c], self.wt[c], self.s[c], K=w["K"], N=w["N"],
+                          layout=w["layout"], flags=flags, out=self.y[c])
+
+
+def copies_for(w, l2_bytes: int) -> int:
+    per = weight_bytes(w)
+    return max(2, int(np.ceil(2.2 * l2_bytes / per)))
+
+
+def time_steps(wl: Workload, steps: int, warmup: int, chunk: int = 256):
+    """Exactly `steps` launches replayed from CUDA graphs; returns (ms, t0, t1)."""
+    import torch
+    chunk = max(1, min(chunk, steps))
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def capture(n, base):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                wl.launch(base + i)
+        return g
+
+    with torch.cuda.stream(stream):
+        for i in range(min(warmup, 8)):
+            wl.launch(i)
+    torch.cuda.synchronize()
+    full = capture(chunk, 0)
+    rem = steps % chunk
+    tail = capture(rem, chunk) if rem else None
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            full.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // chunk):
+            full.replay()
+        if tail is not None:
+            tail.replay()
+        e1.record(stream)
+    e1.synchronize()
+    t1 = time.time()
+    return e0.elapsed_time(e1), t0, t1
+
+
+def time_e2e(w, steps: int):
+    """Public API with host buffers: pinned x -> device, linear, y -> pinned host, every step."""
+    import torch
+    from w4a16_int4_quantized_gb300 import ops, synth
+    M, N, K, G = w["M"], w["N"], w["K"], w["G"]
+    if w["kind"] == "w4a16":
+        x, wp, s = synth.w4a16_inputs(1001, M, N, K, G)
+        xh = torch.from_numpy(x.view(np.int16)).pin_memory()
+        wd = torch.from_numpy(wp).cuda()
+        sd = torch.from_numpy(s.view(np.int16)).cuda()
+        xd = torch.empty_like(xh, device="cuda")
+        yd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+        def step():
+            xd.copy_(xh, non_blocking=True)
+            ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, out=yd)
+            yh.copy_(yd, non_blocking=True)
+        h2d = xh.numel() * 2
+    else:
+        x, W = synth.w4a8_inputs(1001, M, N, K)
+        xh = torch.from_numpy(x).pin_memory()
+        wq, sw = ops.quantize_matrix_q4(torch.from_numpy(W).cuda())
+        xd = torch.empty_like(xh, device="cuda")
+        yd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+
+        def step():
+            xd.copy_(xh, non_blocking=True)
+            xq, sx, _ = ops.quantize_row_q8(xd)
+            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, out=yd)
+            yh.copy_(yd, non_blocking=True)
+        h2d = xh.numel() * 4
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        step()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": steps * weight_bytes(w) / (ms / 1e3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(M * N * 4),
+            "ms_per_step": ms / steps}
+
+
+def extra_lines(l2: int, peak_gbs: float):
+    import torch
+    out = []
+    for name in ("w4a8_gemv_m1", "w4a16_decode_m16_n13312", "w4a16_decode_m1_n13312_il", "w4a8_decode_m16_n13312"):
+        w = WORKLOADS[name]
+        wl = Workload(w, copies_for(w, l2))
+        steps = 2048
+        ms, _, _ = time_steps(wl, steps, 3)
+        gbs = steps * weight_bytes(w) / (ms / 1e3) / 1e9
+        ach = step_bytes(w) / (ms / 1e3 / steps) / 1e9
+        out.append({"workload": name, "desc": w["desc"], "metric": "int4 linear weight GB/s",
+                    "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3 / steps, 3),
+                    "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs,
+                                 "frac": round(ach / peak_gbs, 4)}})
+        del wl
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------- arms
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    total_n, total_s = 0, 0.0
+    per_step = max(0.5, min(20.0, args.cpu_seconds / max(1, args.steps)))
+    for _ in range(args.warmup and 1):
+        time_oracle(w, 0.2)
+    cb = None
+    for _ in range(args.steps):
+        cb, n, el = time_oracle(w, per_step)
+        total_n += n
+        total_s += el
+    value = total_n * weight_bytes(w) / total_s / 1e9
+    cb = dict(cb, value=value, sample=f"{total_n} full oracle calls over {args.steps} steps ({total_s:.1f} s)")
+    line = {"impl": "reference", "metric": "int4 linear weight GB/s (M=1 decode)", "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_s * 1e3 / max(1, total_n), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": args.workload, "desc": w["desc"]},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from w4a16_int4_quantized_gb300 import build
+    if rank == 0:
+        build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    from w4a16_int4_quantized_gb300 import ops
+    torch.cuda.set_device(local)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or L2_FALLBACK)
+    peaks, peak_src = measured_peaks()
+    w = WORKLOADS[args.workload]
+    copies = copies_for(w, l2)
+    wl = Workload(w, copies)
+    ops.device_status(clear=True)
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    ms, t0, t1 = time_steps(wl, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    time.sleep(0.2)
+    sampler.stop()
+    ms_max = ms
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+        dist.barrier()
+    status = ops.device_status()
+    value = world * args.steps * weight_bytes(w) / (ms_max / 1e3) / 1e9
+    per_launch_s = ms / 1e3 / args.steps
+    achieved = step_bytes(w) / per_launch_s / 1e9
+    peak = float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))
+    if rank != 0:
+        return
+    del wl
+    torch.cuda.empty_cache()
+    e2e = time_e2e(w, min(args.steps, 2000))
+    cpu = None
+    if not args.no_cpu:
+        cpu, _, _ = time_oracle(w, args.cpu_seconds)
+    extra = [] if args.no_extra else extra_lines(l2, peak)
+    line = {
+        "metric": "int4 linear weight GB/s (M=1 decode)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w["kind"] == "w4a16" else "s8", "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"], "N": w["N"], "K": w["K"],
+                   "G": w["G"], "parallelism": "replicas" if world > 1 else "single",
+                   "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                         f"({copies * weight_bytes(w) / 2**20:.0f} MiB) vs L2 {l2 / 2**20:.0f} MiB",
+                   "timing": "CUDA events around CUDA-graph replays of exactly `steps` launches"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
+                     "bytes_per_launch": step_bytes(w)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(t0, t1),
+        "device_status": status,
+        "extra": extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=65536)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w4a16_gemv_m1")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

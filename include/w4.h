@@ -1,0 +1,200 @@
+/*
+ * w4.h -- C ABI of libw4gb300: fused int4 dequantize-matmul on GB300 (sm_103a).
+ *
+ * y = x . W^T with a 4-bit W that is never materialised in float.  Two
+ * contracts:
+ *   W4A8 (docs.rs ftts_kernels::int4): symmetric per-output-channel Q4
+ *     codes q in [-7, 7] stored biased u = q + 8, two per byte, low nibble
+ *     first along k, odd K padded with the biased zero 8; activations
+ *     quantized per row to Q8; exact i32 accumulation; two f32 scales
+ *     applied once per element in a fixed order.
+ *   Group-wise W4A16 ("Fused int4 and int8 dequantize-matmul in C",
+ *     sections 2.2-2.3): signed two's-complement nibbles in [-8, 7], one IEEE
+ *     f16 scale per group of G columns, bf16 activations, fp32 accumulation:
+ *     y = sum_g s_g * sum_{k in g} x_k q_k.
+ * and the interleaved [N/64][K][32 B] weight layout of vllm-omni "The 4-bit
+ * CPU path" ("The weight layout, measured"), read in-kernel.
+ *
+ * Conventions shared by every call
+ *   - Pointers are DEVICE pointers owned by the caller, unless stated
+ *     otherwise.  Tensors are dense and row-major.  The library never
+ *     allocates device memory and never frees caller memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call is asynchronous on that stream; results are
+ *     visible after the stream is synchronised.
+ *   - Validation happens on the host before anything is launched or read.
+ *     On any error return nothing is read and every output is left untouched
+ *     ("Fused int4 ..." section 4: errors before any read).  Order of checks:
+ *       1. a negative dimension                          -> W4_EINVAL
+ *       2. a shape the layout cannot describe            -> W4_ESHAPE
+ *       3. M == 0 or N == 0 (rows == 0)                  -> W4_OK, no launch
+ *       4. a required pointer is NULL                    -> W4_EINVAL
+ *       5. K == 0: outputs that are sums are zero-filled -> W4_OK
+ *     A pointer to a buffer that would hold zero elements may be NULL.
+ *   - W4_ECUDA: a CUDA launch or copy failed (the CUDA error is returned by
+ *     w4_last_cuda_error()).
+ *   - Kernels never spin without a bound.  A wait that runs out (about one
+ *     second) sets a bit in the device status word and the kernel returns
+ *     early; read it with w4_device_status().
+ *   - Odd K is accepted for both contracts: a packed row then has
+ *     Kp/2 bytes (Kp = K + 1) and its last high nibble is a pad that is never
+ *     multiplied by a real activation (the kernels treat x[K] as 0).
+ */
+#ifndef W4_H
+#define W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    W4_OK = 0,
+    W4_EINVAL = 1, /* NULL pointer, negative dimension, unknown layout/op, workspace too small */
+    W4_ESHAPE = 2, /* shape the layout cannot describe ("Fused int4 ..." section 4: TL_ESHAPE) */
+    W4_ECUDA = 3   /* a CUDA call failed */
+} w4_status;
+
+/* Weight layouts accepted by the linears. */
+enum {
+    W4_LAYOUT_ROWMAJOR = 0,  /* packed [N][ceil(K/2)] (int4) or [N][K] (int8) */
+    W4_LAYOUT_N64 = 1        /* int4 only: [N/64][K][32 B], byte d = channel d (low) | channel d+32 (high);
+                                requires N % 64 == 0 (vllm-omni "The 4-bit CPU path": the block must tile N) */
+};
+
+/* Launch flags of the linears. */
+enum {
+    /* Programmatic dependent launch: the kernel may start, and begin reading
+     * the weights and scales, while the previous kernel on `stream` is still
+     * running; it waits for that kernel before it reads x or writes y.  Only
+     * set it when no earlier work on the stream that may still be running
+     * writes the weight or scale buffers of this call. */
+    W4_FLAG_PDL = 1u
+};
+
+/* Operation ids for w4_workspace_bytes. */
+enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2 };
+
+/* ---- quantizers ------------------------------------------------------------ */
+
+/* quantize_row_q8 (docs.rs ftts_kernels::int8, module summary and
+ * quantize_row_q8): per row m of x [M][K] (f32), the canonical symmetric Q8
+ * recipe: sx[m] = max_k |x[m][k]| / 127 (one f32 IEEE division);
+ * q[m][k] = clamp(rint(x[m][k] / sx[m]), -127, 127), ties to even; -128 is
+ * never emitted.  A row whose sx is 0 (all zero, or an underflowing max)
+ * gets all-zero codes.  rowsum[m] = sum_k q[m][k] (i32), the activation sum
+ * of the bias correction of dot_i32_q4 (NULL: not written).
+ * Outputs: q [M][K] int8, sx [M] f32, rowsum [M] i32.  NaN/Inf inputs are
+ * unsupported (not checked: checking would read data before validation).
+ * Bit-exact with the CPU definition: same division, same rounding. */
+w4_status w4_quantize_row_q8(const float *x, int64_t M, int64_t K, int8_t *q, float *sx,
+                             int32_t *rowsum, void *stream);
+
+/* quantize_matrix_q4 (docs.rs ftts_kernels::int4, "The quantization
+ * contract" and "Packing"): per output channel n of W [N][K] (f32),
+ * sw[n] = max_k |W[n][k]| / 7, q = clamp(rint(W / sw), -7, 7) (ties to
+ * even; -8 never emitted), stored u = q + 8 in packed [N][ceil(K/2)]:
+ * byte b holds column 2b in bits 0-3 and column 2b+1 in bits 4-7; for odd
+ * K the last high nibble is 8 (the biased zero, which decodes to 0).
+ * A channel with sw == 0 stores all u = 8. */
+w4_status w4_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw,
+                                void *stream);
+
+/* quantize_matrix_q8 (docs.rs ftts_kernels::int8, QuantizedMatrix): the
+ * Q8 recipe of w4_quantize_row_q8 per output channel: q [N][K] int8 in
+ * [-127, 127], sw [N] f32.  Weights for w4_linear_q8. */
+w4_status w4_quantize_matrix_q8(const float *W, int64_t N, int64_t K, int8_t *q, float *sw,
+                                void *stream);
+
+/* ---- dot ------------------------------------------------------------------- */
+
+/* dot_i32_q4 (docs.rs ftts_kernels::int4, dot_i32_q4 and "Packing"):
+ * exact i32 dot of one Q8 activation row xq [K] with one packed biased-Q4
+ * weight row wrow [ceil(K/2)]:  sum_k xq[k]*u[k] - 8 * sum_k xq[k]
+ * (= sum_k xq[k]*(u[k]-8)).  `out` is a device pointer to one int32.
+ * K > 1,127,288 -> W4_ESHAPE (|sum xq*u| could leave i32). */
+w4_status w4_dot_i32_q4(const int8_t *xq, const uint8_t *wrow, int64_t K, int32_t *out, void *stream);
+
+/* ---- linears --------------------------------------------------------------- */
+
+/* linear_q4, W4A8 (docs.rs ftts_kernels::int4, linear_q4; scale order:
+ * docs.rs ftts_kernels::int8 module summary):
+ *   acc[m][n] = sum_k xq[m][k] * (u[n][k] - 8)          exact i32
+ *   y[m][n]   = (f32(acc) * sx[m]) * sw[n]               two f32 multiplies,
+ *                                                        round to nearest even,
+ *                                                        no fused multiply-add
+ * xq [M][K] int8 and sx [M] from w4_quantize_row_q8; w packed biased
+ * nibbles in `layout` (W4_LAYOUT_ROWMAJOR: [N][ceil(K/2)]; W4_LAYOUT_N64:
+ * [N/64][K][32]); sw [N]; y [M][N] f32.  Bit-exact with the CPU oracle for
+ * every M.  Every nibble value decodes (0 -> -8) even though the quantizer
+ * never emits it.
+ * workspace: device scratch of at least w4_workspace_bytes(W4_OP_LINEAR_Q4,
+ * M, N, K, 0) bytes (may be NULL when that is 0); it must not be used by
+ * concurrently running work.  flags: 0 or W4_FLAG_PDL.
+ * ESHAPE: K > 1,000,000; layout N64 with N % 64 != 0.  EINVAL: unknown layout. */
+w4_status w4_linear_q4(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw,
+                       float *y, int64_t M, int64_t N, int64_t K, int32_t layout,
+                       void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
+
+/* linear_q8, W8A8 (docs.rs ftts_kernels::int8, linear_q8): the same
+ * epilogue over acc[m][n] = sum_k xq[m][k] * w[n][k] (exact i32), w [N][K]
+ * int8 (from w4_quantize_matrix_q8), sw [N].  Bit-exact with the oracle.
+ * ESHAPE: K > 131,072 (|acc| could leave i32 for arbitrary int8 weights).
+ * linear_q8_dynamic is the composition w4_quantize_row_q8 + w4_linear_q8. */
+w4_status w4_linear_q8(const int8_t *xq, const float *sx, const int8_t *w, const float *sw,
+                       float *y, int64_t M, int64_t N, int64_t K,
+                       void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
+
+/* linear_w4a16_group ("Fused int4 and int8 dequantize-matmul in C",
+ * sections 2.2-2.3):
+ *   y[m][n] = sum_g s[n][g] * sum_{k in group g} x[m][k] * q[n][k]
+ * x [M][K] bf16 bit patterns; w signed two's-complement nibbles
+ * (q = u - 16 when u >= 8) in `layout`; scales [N][Kp/G] IEEE f16 bit
+ * patterns (Kp = K rounded up to even); y [M][N] f32; fp32 accumulation.
+ * Accuracy (against the exact-product sum):
+ *   |y - y_exact| <= 1e-5 * sum_k |x_k W_nk| + 1e-6        for M <= 16,
+ *   |y - y_exact| <= 4e-3 * sum_k |x_k W_nk| + 1e-6        for M > 16, where
+ * the weight is dequantised once to bf16(q * s) in shared memory and fed to
+ * bf16 tensor-core MMA (vllm-omni "The 4-bit CPU path": large batches
+ * dequantize once and run a dense GEMM).
+ * ESHAPE: G <= 0, G odd, Kp % G != 0 ("Fused int4 ..." section 2.2: G even
+ * and positive, whole groups); layout N64 with N % 64 != 0. */
+w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const uint16_t *scales_f16,
+                                float *y, int64_t M, int64_t N, int64_t K, int64_t G, int32_t layout,
+                                void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
+
+/* ---- layout ---------------------------------------------------------------- */
+
+/* pack_interleaved_n64 (vllm-omni "The 4-bit CPU path", "The weight layout,
+ * measured"): row-major packed int4 [N][ceil(K/2)] -> [N/64][K][32]:
+ * w_il[b][k][d] = nib(64b+d, k) | nib(64b+d+32, k) << 4.  A pure
+ * permutation of nibbles (either encoding).  ESHAPE: N % 64 != 0. */
+w4_status w4_pack_interleaved_n64(const uint8_t *w_rowmajor, uint8_t *w_il, int64_t N, int64_t K,
+                                  void *stream);
+
+/* ---- host queries ---------------------------------------------------------- */
+
+/* Bytes of device scratch the op needs at this shape (0: pass NULL). */
+size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G);
+
+/* Reads (and when clear != 0, clears) the device status word of the
+ * current device: 0 when no kernel has given up on a bounded wait.  Bits:
+ * 1 = a weight-tile copy wait timed out, 2 = a tensor-core pipeline wait
+ * timed out.  Synchronous (a small device-to-host copy). */
+w4_status w4_device_status(uint32_t *out, int32_t clear);
+
+/* The cudaError_t (as int) behind the last W4_ECUDA of this thread. */
+int32_t w4_last_cuda_error(void);
+
+/* Static string for a status code. */
+const char *w4_status_string(w4_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t w4_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* W4_H */

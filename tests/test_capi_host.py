@@ -1,0 +1,108 @@
+"""The C-ABI library on the host: it loads without a GPU, exports every symbol
+include/w4.h declares, and validates arguments before touching the device
+(error order of "Fused int4 and int8 dequantize-matmul in C", section 4:
+EINVAL for negative dims / NULL pointers, ESHAPE for shapes the layout cannot
+describe, M or N == 0 a no-op).  Only calls that fail validation or return
+before any launch run here: no CUDA work is attempted."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w4.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from w4a16_int4_quantized_gb300 import build
+    build.build()
+    from w4a16_int4_quantized_gb300 import ops
+    return ops
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(w4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("w4_quantize_row_q8", "w4_quantize_matrix_q4", "w4_dot_i32_q4", "w4_linear_q4",
+                 "w4_linear_q8", "w4_linear_w4a16_group", "w4_pack_interleaved_n64"):
+        assert name in syms
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert syms
+    missing = [s for s in syms if not hasattr(lib.raw, s)]
+    assert not missing, missing
+    bound = {name for name, _, _ in lib.SIGNATURES}
+    assert set(syms) == bound, set(syms) ^ bound
+
+
+def test_version_and_strings(lib):
+    assert lib.version() >= 100
+    assert lib.raw.w4_status_string(2).decode().startswith("W4_ESHAPE")
+
+
+FAKE = C.c_void_p(0x1000)   # never dereferenced: validation rejects the call first
+
+
+def test_linear_q4_validation(lib):
+    r = lib.raw
+    f = lambda M, N, K, layout=0, y=FAKE, x=FAKE, w=FAKE: r.w4_linear_q4(x, FAKE, w, FAKE, y, M, N, K, layout,
+                                                                          None, 0, 0, None)
+    assert f(-1, 4, 4) == lib.W4_EINVAL
+    assert f(1, -4, 4) == lib.W4_EINVAL
+    assert f(1, 4, -4) == lib.W4_EINVAL
+    assert f(1, 4, 4, layout=7) == lib.W4_EINVAL
+    assert f(1, 65, 4, layout=1) == lib.W4_ESHAPE        # interleaved layout needs N % 64 == 0
+    assert f(1, 4, 2_000_000) == lib.W4_ESHAPE           # i32 accumulator bound
+    assert f(0, 4, 4) == lib.W4_OK                       # M == 0: nothing launched
+    assert f(4, 0, 4) == lib.W4_OK
+    assert f(1, 4, 4, y=None) == lib.W4_EINVAL
+    assert f(1, 4, 4, w=None) == lib.W4_EINVAL
+    assert f(1, 4, 4, x=None) == lib.W4_EINVAL
+
+
+def test_linear_w4a16_validation(lib):
+    r = lib.raw
+    f = lambda M, N, K, G, layout=0, s=FAKE: r.w4_linear_w4a16_group(FAKE, FAKE, s, FAKE, M, N, K, G, layout,
+                                                                      None, 0, 0, None)
+    assert f(1, 2, 4, 3) == lib.W4_ESHAPE     # G odd
+    assert f(1, 2, 4, 0) == lib.W4_ESHAPE     # G <= 0
+    assert f(1, 2, 4, -2) == lib.W4_ESHAPE
+    assert f(1, 2, 12, 8) == lib.W4_ESHAPE    # Kp % G != 0
+    assert f(1, 2, 2047, 48) == lib.W4_ESHAPE  # odd K: Kp = 2048, not a multiple of 48
+    assert f(-1, 2, 4, 2) == lib.W4_EINVAL
+    assert f(0, 2, 4, 2) == lib.W4_OK
+    assert f(1, 2, 4, 2, s=None) == lib.W4_EINVAL
+    assert f(1, 65, 4, 2, layout=1) == lib.W4_ESHAPE
+
+
+def test_other_validation(lib):
+    r = lib.raw
+    assert r.w4_quantize_row_q8(FAKE, -1, 4, FAKE, FAKE, None, None) == lib.W4_EINVAL
+    assert r.w4_quantize_row_q8(FAKE, 0, 4, FAKE, FAKE, None, None) == lib.W4_OK
+    assert r.w4_quantize_row_q8(FAKE, 2, 4, FAKE, None, None, None) == lib.W4_EINVAL
+    assert r.w4_quantize_matrix_q4(FAKE, 3, -1, FAKE, FAKE, None) == lib.W4_EINVAL
+    assert r.w4_quantize_matrix_q4(None, 0, 8, None, None, None) == lib.W4_OK
+    assert r.w4_quantize_matrix_q8(FAKE, 3, 4, FAKE, None, None) == lib.W4_EINVAL
+    assert r.w4_dot_i32_q4(FAKE, FAKE, -1, FAKE, None) == lib.W4_EINVAL
+    assert r.w4_dot_i32_q4(FAKE, FAKE, 2_000_000, FAKE, None) == lib.W4_ESHAPE
+    assert r.w4_dot_i32_q4(FAKE, FAKE, 8, None, None) == lib.W4_EINVAL
+    assert r.w4_pack_interleaved_n64(FAKE, FAKE, 100, 8, None) == lib.W4_ESHAPE
+    assert r.w4_pack_interleaved_n64(FAKE, FAKE, 0, 8, None) == lib.W4_OK
+    assert r.w4_linear_q8(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 200_000, None, 0, 0, None) == lib.W4_ESHAPE
+    assert r.w4_linear_q8(FAKE, FAKE, FAKE, FAKE, None, 1, 4, 8, None, 0, 0, None) == lib.W4_EINVAL
+    assert r.w4_device_status(None, 0) == lib.W4_EINVAL
+
+
+def test_workspace_query_is_host_only(lib):
+    for op in (lib.OP_LINEAR_Q4, lib.OP_LINEAR_Q8, lib.OP_LINEAR_W4A16):
+        assert lib.workspace_bytes(op, 1, 2048, 2048, 128) == 0        # decode needs no scratch
+        assert lib.workspace_bytes(op, 2048, 2048, 2048, 128) >= 0

@@ -1,0 +1,218 @@
+// capi.cu -- the extern "C" boundary of libw4gb300 (declared in include/w4.h).
+//
+// Host-side validation happens here, before anything is launched or read,
+// in the order the header documents; then each call is routed to one CUDA
+// path: the quantizers, the decode GEMV (M <= 16), the tcgen05 prefill GEMM
+// (M > 16, shapes it can tile) or the generic kernel (anything else).  There
+// is no CPU fallback: every result comes from a kernel.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/w4.h"
+#include "internal.h"
+
+namespace {
+
+__device__ uint32_t g_status_word;
+
+thread_local int32_t t_last_cuda_error = 0;
+
+w4_status cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return W4_OK;
+    t_last_cuda_error = (int32_t)e;
+    return W4_ECUDA;
+}
+
+// Device address of the status word on the current device (resolved once per device).
+cudaError_t status_ptr(uint32_t **out) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<uint32_t *> cache[kMaxDev];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    uint32_t *p = cache[dev].load(std::memory_order_acquire);
+    if (!p) {
+        std::lock_guard<std::mutex> lk(mu);
+        p = cache[dev].load(std::memory_order_relaxed);
+        if (!p) {
+            void *addr = nullptr;
+            e = cudaGetSymbolAddress(&addr, g_status_word);
+            if (e != cudaSuccess) return e;
+            p = static_cast<uint32_t *>(addr);
+            cache[dev].store(p, std::memory_order_release);
+        }
+    }
+    *out = p;
+    return cudaSuccess;
+}
+
+inline cudaStream_t as_stream(void *s) { return static_cast<cudaStream_t>(s); }
+
+constexpr int64_t kMaxKQ4 = 1000000;        // |sum xq*u| < 2^31 needs K <= 1,127,288
+constexpr int64_t kMaxKQ8 = 131072;         // |sum xq*w| < 2^31 for any int8 weights needs K <= 133,144
+constexpr int64_t kMaxKDot = 1127288;
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+w4_status run_linear(w4::LinearArgs &a, cudaStream_t st) {
+    uint32_t *status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_status(e);
+    a.status = status;
+    if (a.M <= 16 && w4::gemv_supported(a)) return cuda_status(w4::launch_gemv(a, st));
+    if (a.M > 16 && w4::gemm_supported(a)) return cuda_status(w4::launch_gemm(a, st));
+    return cuda_status(w4::launch_generic(a, st));
+}
+
+w4_status check_workspace(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G, void *ws, size_t ws_bytes) {
+    const size_t need = w4_workspace_bytes(op, M, N, K, G);
+    if (need > ws_bytes) return W4_EINVAL;
+    if (need > 0 && ws == nullptr) return W4_EINVAL;
+    return W4_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+w4_status w4_quantize_row_q8(const float *x, int64_t M, int64_t K, int8_t *q, float *sx, int32_t *rowsum,
+                             void *stream) {
+    if (M < 0 || K < 0) return W4_EINVAL;
+    if (M >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (M == 0) return W4_OK;
+    if (!sx || (K > 0 && (!x || !q))) return W4_EINVAL;
+    return cuda_status(w4::launch_quantize_rows(x, M, K, 127, q, sx, rowsum, as_stream(stream)));
+}
+
+w4_status w4_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw, void *stream) {
+    if (N < 0 || K < 0) return W4_EINVAL;
+    if (N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (N == 0) return W4_OK;
+    if (!sw || (K > 0 && (!W || !packed))) return W4_EINVAL;
+    return cuda_status(w4::launch_quantize_matrix_q4(W, N, K, packed, sw, as_stream(stream)));
+}
+
+w4_status w4_quantize_matrix_q8(const float *W, int64_t N, int64_t K, int8_t *q, float *sw, void *stream) {
+    if (N < 0 || K < 0) return W4_EINVAL;
+    if (N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (N == 0) return W4_OK;
+    if (!sw || (K > 0 && (!W || !q))) return W4_EINVAL;
+    return cuda_status(w4::launch_quantize_rows(W, N, K, 127, q, sw, nullptr, as_stream(stream)));
+}
+
+w4_status w4_dot_i32_q4(const int8_t *xq, const uint8_t *wrow, int64_t K, int32_t *out, void *stream) {
+    if (K < 0) return W4_EINVAL;
+    if (K > kMaxKDot) return W4_ESHAPE;
+    if (!out || (K > 0 && (!xq || !wrow))) return W4_EINVAL;
+    if (K == 0) return cuda_status(cudaMemsetAsync(out, 0, sizeof(int32_t), as_stream(stream)));
+    return cuda_status(w4::launch_dot_i32_q4(xq, wrow, K, out, as_stream(stream)));
+}
+
+w4_status w4_linear_q4(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw, float *y, int64_t M,
+                       int64_t N, int64_t K, int32_t layout, void *workspace, size_t ws_bytes, uint32_t flags,
+                       void *stream) {
+    if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64) return W4_EINVAL;
+    if (K > kMaxKQ4 || M >= kMaxDim || N >= kMaxDim) return W4_ESHAPE;
+    if (layout == W4_LAYOUT_N64 && N % 64) return W4_ESHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y || !sx || !sw || (K > 0 && (!xq || !w))) return W4_EINVAL;
+    const w4_status ws = check_workspace(W4_OP_LINEAR_Q4, M, N, K, 0, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), as_stream(stream)));
+    w4::LinearArgs a = {};
+    a.kind = w4::KIND_W4A8;
+    a.x = xq; a.w = w; a.scale = sw; a.sx = sx; a.y = y;
+    a.M = M; a.N = N; a.K = K; a.G = 0; a.layout = layout; a.flags = flags;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    return run_linear(a, as_stream(stream));
+}
+
+w4_status w4_linear_q8(const int8_t *xq, const float *sx, const int8_t *w, const float *sw, float *y, int64_t M,
+                       int64_t N, int64_t K, void *workspace, size_t ws_bytes, uint32_t flags, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (K > kMaxKQ8 || M >= kMaxDim || N >= kMaxDim) return W4_ESHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y || !sx || !sw || (K > 0 && (!xq || !w))) return W4_EINVAL;
+    const w4_status ws = check_workspace(W4_OP_LINEAR_Q8, M, N, K, 0, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), as_stream(stream)));
+    w4::LinearArgs a = {};
+    a.kind = w4::KIND_W8A8;
+    a.x = xq; a.w = reinterpret_cast<const uint8_t *>(w); a.scale = sw; a.sx = sx; a.y = y;
+    a.M = M; a.N = N; a.K = K; a.G = 0; a.layout = W4_LAYOUT_ROWMAJOR; a.flags = flags;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    return run_linear(a, as_stream(stream));
+}
+
+w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const uint16_t *scales_f16, float *y,
+                                int64_t M, int64_t N, int64_t K, int64_t G, int32_t layout, void *workspace,
+                                size_t ws_bytes, uint32_t flags, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64) return W4_EINVAL;
+    const int64_t Kp = K + (K & 1);
+    if (G <= 0 || (G & 1) || (Kp % G) != 0) return W4_ESHAPE;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (layout == W4_LAYOUT_N64 && N % 64) return W4_ESHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y || (K > 0 && (!x_bf16 || !w || !scales_f16))) return W4_EINVAL;
+    const w4_status ws = check_workspace(W4_OP_LINEAR_W4A16, M, N, K, G, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), as_stream(stream)));
+    w4::LinearArgs a = {};
+    a.kind = w4::KIND_W4A16;
+    a.x = x_bf16; a.w = w; a.scale = scales_f16; a.sx = nullptr; a.y = y;
+    a.M = M; a.N = N; a.K = K; a.G = G; a.layout = layout; a.flags = flags;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    return run_linear(a, as_stream(stream));
+}
+
+w4_status w4_pack_interleaved_n64(const uint8_t *w_rowmajor, uint8_t *w_il, int64_t N, int64_t K, void *stream) {
+    if (N < 0 || K < 0) return W4_EINVAL;
+    if (N % 64) return W4_ESHAPE;
+    if (N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (N == 0 || K == 0) return W4_OK;
+    if (!w_rowmajor || !w_il) return W4_EINVAL;
+    return cuda_status(w4::launch_pack_n64(w_rowmajor, w_il, N, K, as_stream(stream)));
+}
+
+size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G) {
+    if (M <= 16 || N <= 0 || K <= 0) return 0;
+    switch (op) {
+        case W4_OP_LINEAR_Q4: return w4::gemm_workspace_bytes(w4::KIND_W4A8, M, N, K, G);
+        case W4_OP_LINEAR_Q8: return w4::gemm_workspace_bytes(w4::KIND_W8A8, M, N, K, G);
+        case W4_OP_LINEAR_W4A16: return w4::gemm_workspace_bytes(w4::KIND_W4A16, M, N, K, G);
+        default: return 0;
+    }
+}
+
+w4_status w4_device_status(uint32_t *out, int32_t clear) {
+    if (!out) return W4_EINVAL;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_status_word, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_status(e);
+    if (clear) {
+        const uint32_t zero = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_status(e);
+    }
+    return W4_OK;
+}
+
+int32_t w4_last_cuda_error(void) { return t_last_cuda_error; }
+
+const char *w4_status_string(w4_status s) {
+    switch (s) {
+        case W4_OK: return "W4_OK";
+        case W4_EINVAL: return "W4_EINVAL: invalid argument";
+        case W4_ESHAPE: return "W4_ESHAPE: shape not supported by the layout";
+        case W4_ECUDA: return "W4_ECUDA: CUDA call failed";
+        default: return "unknown w4_status";
+    }
+}
+
+int32_t w4_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// internal.h -- launchers shared between the kernel translation units and the C ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4 {
+
+enum Kind : int { KIND_W4A8 = 0, KIND_W8A8 = 1, KIND_W4A16 = 2 };
+
+// One linear call after host validation (shapes legal, pointers non-NULL,
+// M, N, K > 0).
+struct LinearArgs {
+    int kind;
+    const void *x;       // int8 [M][K] (W4A8, W8A8) or bf16 [M][K] (W4A16)
+    const uint8_t *w;    // packed int4 (layout) or int8 [N][K]
+    const void *scale;   // f32 sw [N] (int kinds) or f16 [N][Kp/G] (W4A16)
+    const float *sx;     // f32 [M] (int kinds)
+    float *y;            // f32 [M][N]
+    int64_t M, N, K, G;  // G: W4A16 only
+    int layout;          // 0 row-major, 1 interleaved [N/64][K][32]
+    uint32_t flags;      // W4_FLAG_PDL
+    void *workspace;
+    size_t ws_bytes;
+    uint32_t *status;    // device status word
+};
+
+// quant.cu
+cudaError_t launch_quantize_rows(const float *x, int64_t rows, int64_t K, int Q, int8_t *q, float *s,
+                                 int32_t *rowsum, cudaStream_t st);
+cudaError_t launch_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw,
+                                      cudaStream_t st);
+cudaError_t launch_dot_i32_q4(const int8_t *xq, const uint8_t *wrow, int64_t K, int32_t *out, cudaStream_t st);
+cudaError_t launch_pack_n64(const uint8_t *w, uint8_t *il, int64_t N, int64_t K, cudaStream_t st);
+
+// gemv.cu -- small-M tensor-core GEMV (M <= 16) and the generic fallback.
+bool gemv_supported(const LinearArgs &a);
+cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st);
+cudaError_t launch_generic(const LinearArgs &a, cudaStream_t st);
+
+// gemm_tc.cu -- tcgen05 prefill GEMM (M > 16).
+bool gemm_supported(const LinearArgs &a);
+size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K, int64_t G);
+cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st);
+
+}  // namespace w4

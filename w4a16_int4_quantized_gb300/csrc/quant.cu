@@ -1,0 +1,180 @@
+// quant.cu -- quantizers, the single-row biased-Q4 dot, and the interleave packer.
+//
+// quantize_row_q8 / quantize_matrix_q8 / quantize_matrix_q4 follow the
+// canonical symmetric recipe of docs.rs ftts_kernels::int8 (module summary,
+// quantize_row_q8) and its Q4 counterpart in ftts_kernels::int4 ("The
+// quantization contract", "Packing"): s = max|row| / Q by one IEEE f32
+// division, codes = clamp(rint(v / s), -Q, Q) with ties to even.  The
+// kernels use __fdiv_rn and __float2int_rn (IEEE round-to-nearest-even) and
+// max via fmaxf, which is exact and order-free, so their codes and scales
+// are bit-identical to the CPU definition.
+#include "common.cuh"
+#include "internal.h"
+
+#include <algorithm>
+
+namespace w4 {
+namespace {
+
+constexpr int kThreads = 256;
+
+W4_DEV float block_max(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float r = red[0];
+    __syncthreads();
+    return r;
+}
+
+W4_DEV int block_sum_i32(int v, int *red) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < (int)(blockDim.x >> 5) ? red[lane] : 0;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const int r = red[0];
+    __syncthreads();
+    return r;
+}
+
+// One code of the symmetric recipe (s > 0).
+W4_DEV int quant_code(float v, float s, int Q) {
+    int q = __float2int_rn(__fdiv_rn(v, s));
+    return min(max(q, -Q), Q);
+}
+
+// One CTA per row: max|v|, the scale, the codes, and (optionally) their sum.
+__global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *__restrict__ x, int64_t K, int Q,
+                                                                 int8_t *__restrict__ q, float *__restrict__ s,
+                                                                 int32_t *__restrict__ rowsum) {
+    __shared__ float redf[32];
+    __shared__ int redi[32];
+    const int64_t row = blockIdx.x;
+    const float *xr = x + row * K;
+    float amax = 0.0f;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(xr[k]));
+    amax = block_max(amax, redf);
+    const float sc = __fdiv_rn(amax, (float)Q);
+    if (threadIdx.x == 0) s[row] = sc;
+    int8_t *qr = q + row * K;
+    int sum = 0;
+    if (sc == 0.0f) {
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) qr[k] = 0;
+    } else {
+        for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
+            const int c = quant_code(xr[k], sc, Q);
+            qr[k] = (int8_t)c;
+            sum += c;
+        }
+    }
+    if (rowsum) {
+        sum = block_sum_i32(sum, redi);
+        if (threadIdx.x == 0) rowsum[row] = sum;
+    }
+}
+
+// One CTA per output channel: Q4 codes stored u = q + 8, two per byte, low
+// nibble = even column; odd K pads the last high nibble with 8.
+__global__ void __launch_bounds__(kThreads) quantize_q4_kernel(const float *__restrict__ W, int64_t K,
+                                                               uint8_t *__restrict__ packed, float *__restrict__ sw) {
+    __shared__ float redf[32];
+    const int64_t row = blockIdx.x;
+    const float *wr = W + row * K;
+    const int64_t Kb = (K + 1) >> 1;
+    float amax = 0.0f;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(wr[k]));
+    amax = block_max(amax, redf);
+    const float sc = __fdiv_rn(amax, 7.0f);
+    if (threadIdx.x == 0) sw[row] = sc;
+    uint8_t *pr = packed + row * Kb;
+    for (int64_t b = threadIdx.x; b < Kb; b += blockDim.x) {
+        const int64_t k = 2 * b;
+        int lo = 8, hi = 8;
+        if (sc != 0.0f) {
+            lo = quant_code(wr[k], sc, 7) + 8;
+            if (k + 1 < K) hi = quant_code(wr[k + 1], sc, 7) + 8;
+        }
+        pr[b] = (uint8_t)(lo | (hi << 4));
+    }
+}
+
+// dot_i32_q4: sum xq*u - 8 * sum xq over one row, exact in i32.
+__global__ void __launch_bounds__(kThreads) dot_q4_kernel(const int8_t *__restrict__ xq,
+                                                          const uint8_t *__restrict__ w, int64_t K,
+                                                          int32_t *__restrict__ out) {
+    __shared__ int redi[32];
+    int sxu = 0, sx = 0;
+    for (int64_t k = threadIdx.x; k < K; k += blockDim.x) {
+        const int x = xq[k];
+        const int u = (w[k >> 1] >> ((k & 1) * 4)) & 0xF;
+        sxu += x * u;
+        sx += x;
+    }
+    sxu = block_sum_i32(sxu, redi);
+    sx = block_sum_i32(sx, redi);
+    if (threadIdx.x == 0) *out = sxu - 8 * sx;
+}
+
+// [N/64][K][32]: byte d of (block b, column k) = nib(64b+d, k) | nib(64b+d+32, k) << 4.
+__global__ void pack_n64_kernel(const uint8_t *__restrict__ w, uint8_t *__restrict__ il, int64_t N, int64_t K) {
+    const int64_t total = (N / 64) * K * 32;
+    const int64_t Kb = (K + 1) >> 1;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i / (K * 32);
+        const int64_t rem = i - b * K * 32;
+        const int64_t k = rem >> 5;
+        const int d = (int)(rem & 31);
+        const int64_t n0 = 64 * b + d;
+        const int sh = (int)(k & 1) * 4;
+        const unsigned lo = (w[n0 * Kb + (k >> 1)] >> sh) & 0xFu;
+        const unsigned hi = (w[(n0 + 32) * Kb + (k >> 1)] >> sh) & 0xFu;
+        il[i] = (uint8_t)(lo | (hi << 4));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_rows(const float *x, int64_t rows, int64_t K, int Q, int8_t *q, float *s,
+                                 int32_t *rowsum, cudaStream_t st) {
+    if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    quantize_rows_kernel<<<(unsigned)rows, kThreads, 0, st>>>(x, K, Q, q, s, rowsum);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw,
+                                      cudaStream_t st) {
+    if (N > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    quantize_q4_kernel<<<(unsigned)N, kThreads, 0, st>>>(W, K, packed, sw);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dot_i32_q4(const int8_t *xq, const uint8_t *wrow, int64_t K, int32_t *out, cudaStream_t st) {
+    dot_q4_kernel<<<1, kThreads, 0, st>>>(xq, wrow, K, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_n64(const uint8_t *w, uint8_t *il, int64_t N, int64_t K, cudaStream_t st) {
+    const int64_t total = (N / 64) * K * 32;
+    const int64_t blocks = std::min<int64_t>(ceil_div(total, 256), 152 * 32);
+    pack_n64_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, il, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace w4

@@ -1,0 +1,202 @@
+"""Thin Python binding over the C ABI of libw4gb300 (include/w4.h).
+
+Argument marshalling only: every function passes torch tensors' device
+pointers, sizes and the current CUDA stream to the ``w4_*`` entry point of
+the same name, and raises ``W4Error`` on a non-OK status.  All arithmetic
+runs in the library's CUDA kernels; if the library is missing this module
+raises on import of the first call -- there is no CPU fallback.
+
+``raw`` is the ctypes handle itself, for callers (and tests) that want to
+drive the C functions with plain pointers.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw4gb300.so")
+
+W4_OK, W4_EINVAL, W4_ESHAPE, W4_ECUDA = 0, 1, 2, 3
+LAYOUT_ROWMAJOR, LAYOUT_N64 = 0, 1
+FLAG_PDL = 1
+OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16 = 0, 1, 2
+
+# (name, restype, argtypes) of every exported symbol, in header order.
+_vp, _i64, _i32, _u32, _sz = C.c_void_p, C.c_int64, C.c_int32, C.c_uint32, C.c_size_t
+SIGNATURES = [
+    ("w4_quantize_row_q8", _i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp]),
+    ("w4_quantize_matrix_q4", _i32, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    ("w4_quantize_matrix_q8", _i32, [_vp, _i64, _i64, _vp, _vp, _vp]),
+    ("w4_dot_i32_q4", _i32, [_vp, _vp, _i64, _vp, _vp]),
+    ("w4_linear_q4", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
+    ("w4_linear_q8", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
+    ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
+    ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
+    ("w4_workspace_bytes", _sz, [_i32, _i64, _i64, _i64, _i64]),
+    ("w4_device_status", _i32, [_vp, _i32]),
+    ("w4_last_cuda_error", _i32, []),
+    ("w4_status_string", C.c_char_p, [_i32]),
+    ("w4_version", _i32, []),
+]
+
+
+class W4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = raw.w4_status_string(status).decode() if raw is not None else str(status)
+        if status == W4_ECUDA and raw is not None:
+            msg += f" (cudaError {raw.w4_last_cuda_error()})"
+        super().__init__(f"{what}: {msg}")
+
+
+def load(path: str = LIB_PATH) -> C.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"libw4gb300 not built ({path}); run __graft_entry__.build() or "
+                           "python -m w4a16_int4_quantized_gb300.build")
+    lib = C.CDLL(path)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+raw = load()
+
+
+def _check(status: int, what: str) -> None:
+    if status != W4_OK:
+        raise W4Error(status, what)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr() or None
+
+
+def _stream(stream=None) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream or None
+
+
+# ---------------------------------------------------------------- quantizers
+
+def quantize_row_q8(x: torch.Tensor, stream=None):
+    """x f32 [M, K] (cuda) -> (q int8 [M, K], sx f32 [M], rowsum int32 [M])."""
+    assert x.dtype == torch.float32 and x.is_contiguous() and x.dim() == 2
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    sx = torch.empty(M, dtype=torch.float32, device=x.device)
+    rs = torch.empty(M, dtype=torch.int32, device=x.device)
+    _check(raw.w4_quantize_row_q8(_ptr(x), M, K, _ptr(q), _ptr(sx), _ptr(rs), _stream(stream)),
+           "w4_quantize_row_q8")
+    return q, sx, rs
+
+
+def quantize_matrix_q4(W: torch.Tensor, stream=None):
+    """W f32 [N, K] -> (packed uint8 [N, ceil(K/2)], sw f32 [N])."""
+    assert W.dtype == torch.float32 and W.is_contiguous() and W.dim() == 2
+    N, K = W.shape
+    packed = torch.empty((N, (K + 1) // 2), dtype=torch.uint8, device=W.device)
+    sw = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check(raw.w4_quantize_matrix_q4(_ptr(W), N, K, _ptr(packed), _ptr(sw), _stream(stream)),
+           "w4_quantize_matrix_q4")
+    return packed, sw
+
+
+def quantize_matrix_q8(W: torch.Tensor, stream=None):
+    """W f32 [N, K] -> (q int8 [N, K], sw f32 [N])."""
+    assert W.dtype == torch.float32 and W.is_contiguous() and W.dim() == 2
+    N, K = W.shape
+    q = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    sw = torch.empty(N, dtype=torch.float32, device=W.device)
+    _check(raw.w4_quantize_matrix_q8(_ptr(W), N, K, _ptr(q), _ptr(sw), _stream(stream)), "w4_quantize_matrix_q8")
+    return q, sw
+
+
+# ---------------------------------------------------------------- dot / linears
+
+def dot_i32_q4(xq: torch.Tensor, wrow: torch.Tensor, K: int | None = None, stream=None) -> torch.Tensor:
+    """Exact biased-Q4 dot of one row -> int32 device scalar."""
+    K = xq.numel() if K is None else K
+    out = torch.empty(1, dtype=torch.int32, device=xq.device)
+    _check(raw.w4_dot_i32_q4(_ptr(xq), _ptr(wrow), K, _ptr(out), _stream(stream)), "w4_dot_i32_q4")
+    return out
+
+
+def _workspace(op, M, N, K, G, workspace, device):
+    need = raw.w4_workspace_bytes(op, M, N, K, G)
+    if need == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace, workspace.numel()
+
+
+def linear_q4(xq, sx, w, sw, K: int | None = None, N: int | None = None, layout: int = LAYOUT_ROWMAJOR,
+              flags: int = 0, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """W4A8: y[M, N] = (f32(sum xq * (u - 8)) * sx[m]) * sw[n]."""
+    M = xq.shape[0]
+    K = xq.shape[1] if K is None else K
+    N = sw.numel() if N is None else N
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    ws, wsb = _workspace(OP_LINEAR_Q4, M, N, K, 0, workspace, xq.device)
+    _check(raw.w4_linear_q4(_ptr(xq), _ptr(sx), _ptr(w), _ptr(sw), _ptr(y), M, N, K, layout,
+                            _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_q4")
+    return y
+
+
+def linear_q8(xq, sx, w, sw, flags: int = 0, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """W8A8: y[M, N] = (f32(sum xq * w) * sx[m]) * sw[n]."""
+    M, K = xq.shape
+    N = w.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    ws, wsb = _workspace(OP_LINEAR_Q8, M, N, K, 0, workspace, xq.device)
+    _check(raw.w4_linear_q8(_ptr(xq), _ptr(sx), _ptr(w), _ptr(sw), _ptr(y), M, N, K,
+                            _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_q8")
+    return y
+
+
+def linear_w4a16_group(x, w, scales, G: int, K: int | None = None, N: int | None = None,
+                       layout: int = LAYOUT_ROWMAJOR, flags: int = 0, out=None, workspace=None,
+                       stream=None) -> torch.Tensor:
+    """Group-wise W4A16: y = sum_g s[n, g] * sum_{k in g} x[m, k] * q[n, k].
+
+    x: bf16 [M, K] (torch.bfloat16, or int16/uint16 bit patterns);
+    w: packed signed nibbles; scales: f16 [N, Kp/G] (torch.float16 or 16-bit patterns).
+    """
+    assert x.element_size() == 2 and scales.element_size() == 2
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    N = scales.shape[0] if N is None else N
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(OP_LINEAR_W4A16, M, N, K, G, workspace, x.device)
+    _check(raw.w4_linear_w4a16_group(_ptr(x), _ptr(w), _ptr(scales), _ptr(y), M, N, K, G, layout,
+                                     _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_w4a16_group")
+    return y
+
+
+def pack_interleaved_n64(w: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+    """Row-major packed int4 [N, ceil(K/2)] -> interleaved [N/64, K, 32]."""
+    N = w.shape[0]
+    il = torch.empty((N // 64, K, 32), dtype=torch.uint8, device=w.device)
+    _check(raw.w4_pack_interleaved_n64(_ptr(w), _ptr(il), N, K, _stream(stream)), "w4_pack_interleaved_n64")
+    return il
+
+
+def workspace_bytes(op: int, M: int, N: int, K: int, G: int = 0) -> int:
+    return int(raw.w4_workspace_bytes(op, M, N, K, G))
+
+
+def device_status(clear: bool = False) -> int:
+    v = C.c_uint32(0)
+    _check(raw.w4_device_status(C.byref(v), 1 if clear else 0), "w4_device_status")
+    return int(v.value)
+
+
+def version() -> int:
+    return int(raw.w4_version())
