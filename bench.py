@@ -48,6 +48,10 @@ WORKLOADS = {
                          desc="W4A8 linear_q4 GEMV, M=1, K=N=2048, per-channel Q4, per-row Q8 x"),
     "w4a16_decode_m16_n13312": dict(kind="w4a16", M=16, N=13312, K=2048, G=128, layout=0,
                                     desc="W4A16 decode batch M=16, K=2048, N=13312, G=128"),
+    "w4a16_decode_m1_n13312": dict(kind="w4a16", M=1, N=13312, K=2048, G=128, layout=0,
+                                   desc="W4A16 M=1, K=2048, N=13312 (gate_up shape), G=128"),
+    "w4a8_decode_m1_n13312": dict(kind="w4a8", M=1, N=13312, K=2048, G=0, layout=0,
+                                  desc="W4A8 M=1, K=2048, N=13312 (gate_up shape)"),
     "w4a16_decode_m1_n13312_il": dict(kind="w4a16", M=1, N=13312, K=2048, G=128, layout=1,
                                       desc="W4A16 M=1, K=2048, N=13312, G=128, interleaved [N/64][K][32] layout"),
     "w4a8_decode_m16_n13312": dict(kind="w4a8", M=16, N=13312, K=2048, G=0, layout=0,

@@ -10,7 +10,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/w4.h"
+#include "w4.h"
 #include "internal.h"
 
 namespace {

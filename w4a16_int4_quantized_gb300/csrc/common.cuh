@@ -87,6 +87,15 @@ W4_DEV void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) 
         : "memory");
 }
 
+// 2-D tiled TMA load of box (c0, c1) of `map` into shared memory, completing
+// the box's bytes on `bar`.  c0 * element size must be a multiple of 16.
+W4_DEV void tma_load_2d(void *dst, const void *map, int c0, int c1, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- PDL
 
 W4_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -39,9 +39,10 @@
 
 #include <algorithm>
 #include <mutex>
+#include <numeric>
 #include <type_traits>
 
-#include "../../include/w4.h"
+#include "w4.h"
 #include "common.cuh"
 #include "internal.h"
 
@@ -61,13 +62,16 @@ struct GemvParams {
     int cpg;         // 32-column chunks per unit (a unit is one group for W4A16, one chunk otherwise)
     int units;       // units per row
     int upc;         // units per CTA (split-K granularity)
+    int upp;         // units per transpose phase (interleaved layout)
     int R, WR, WK;   // rows per CTA, warps along rows, warps along K
     int unit_k;      // columns per unit
     int unit_bytes;  // packed bytes per unit per row
-    int wstride;     // shared row stride of the weight tile (bytes)
+    int wstride;     // shared row stride of the (row-major) weight tile (bytes)
     int xstride;     // shared row stride of the activation tile (bytes)
-    int raw_off, w_off, x_off, sc_off, red_off, xsum_off, flag_off;
+    int sstride;     // shared row stride of the f32 scale tile (floats)
+    int raw_off, w_off, x_off, sc_off, red_off;
     int x_vec;       // activation rows can be read with aligned vector loads
+    int s_vec;       // scale rows can be read as 16-byte vectors
 };
 
 // ---------------------------------------------------------------- MMA wrappers
@@ -102,15 +106,166 @@ W4_DEV void unpack_signed_bf16(uint32_t w, uint32_t (&p)[4]) {
     }
 }
 
-// ---------------------------------------------------------------- kernel
+// 4x4 byte transpose + nibble repack of the interleaved layout: raw rows
+// [k][32 B] (byte d = channel d | channel d+32 << 4) of 8 consecutive k for
+// channels 4*dq..4*dq+3 -> one packed row-major word (8 nibbles, low first)
+// for each of the channels 4*dq+c (lo[c]) and 4*dq+c+32 (hi[c]).
+W4_DEV void deinterleave8(const uint8_t *raw, int dq, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint32_t *>(raw + i * 32 + 4 * dq);
+    uint32_t T[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t a01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x5140);
+        const uint32_t b01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x7362);
+        const uint32_t a23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x5140);
+        const uint32_t b23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x7362);
+        T[h][0] = prmt(a01, a23, 0x5410);  // byte i = column 4h+i of channel 4dq+0
+        T[h][1] = prmt(a01, a23, 0x7632);
+        T[h][2] = prmt(b01, b23, 0x5410);
+        T[h][3] = prmt(b01, b23, 0x7632);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t la = T[0][c] & 0x0F0F0F0Fu, lb = T[1][c] & 0x0F0F0F0Fu;
+        const uint32_t ha = (T[0][c] >> 4) & 0x0F0F0F0Fu, hb = (T[1][c] >> 4) & 0x0F0F0F0Fu;
+        lo[c] = prmt(la | (la >> 4), lb | (lb >> 4), 0x6420);
+        hi[c] = prmt(ha | (ha >> 4), hb | (hb >> 4), 0x6420);
+    }
+}
 
-template <int KIND, bool N64, int RB, int MT>
+// Biased nibbles (u = q + 8) of a word -> four f16x2 pairs of the exact
+// integers q: P0 = (k0, k4), P1 = (k1, k5), P2 = (k2, k6), P3 = (k3, k7).
+// 0x6400 | u is the f16 1024 + u; subtracting 1032 is exact.
+W4_DEV void unpack_biased_f16(uint32_t w, uint32_t (&p)[4]) {
+    const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6408), __ushort_as_half((unsigned short)0x6408));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
+        __half2 h = *reinterpret_cast<const __half2 *>(&v);
+        h = __hsub2(h, off);
+        p[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
+// Eight int8 values (lo = bytes 0-3, hi = bytes 4-7) -> four f16x2 pairs of
+// the same integers, pair i made of the two bytes PRMT selector sel[i] puts
+// in result bytes 0 and 2.  b ^ 0x80 = b + 128; 0x6400 | (b + 128) is the
+// f16 1024 + 128 + b, and subtracting 1152 is exact.
+W4_DEV void s8_to_f16_pairs(uint32_t lo, uint32_t hi, const uint32_t (&sel)[4], uint32_t (&p)[4]) {
+    const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6480), __ushort_as_half((unsigned short)0x6480));
+    lo ^= 0x80808080u;
+    hi ^= 0x80808080u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = (prmt(lo, hi, sel[i]) & 0x00FF00FFu) | 0x64006400u;
+        __half2 h = *reinterpret_cast<const __half2 *>(&v);
+        h = __hsub2(h, off);
+        p[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
+W4_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Division by a CTA-invariant divisor d (< 2^16) of j < 2^16: floor(j / d)
+// = umulhi(j, ceil(2^32 / d)).
+W4_DEV uint32_t div_magic(uint32_t d) { return 0xFFFFFFFFu / d + 1u; }
+W4_DEV int fast_div(int j, uint32_t magic) { return (int)__umulhi((uint32_t)j, magic); }
+
+// One unit (CPG chunks of 32 columns) of one warp: MMA partial sums for the
+// warp's 16-row block (rows g, g + 8 of each thread) against MT 8-row
+// activation tiles.  wr0 / wr8: the thread's word in the unit's first chunk
+// of rows g and g + 8; xr[mt]: the thread's 8 activations of that chunk.
+// Byte offset, inside a weight tile, of the thread's word of 16-byte chunk c
+// of its row.  Row-major tiles arrive by TMA with the 128-byte swizzle:
+// [segment][R rows][128 B], chunk (c mod 8) of a row stored at (c mod 8) xor
+// (row mod 8); a warp's 8 rows then read 8 distinct bank groups.  The
+// interleaved layout is transposed into padded rows of `wstride` bytes.
+template <bool SWZ, int KIND>
+W4_DEV int wword_off(int c, int g, int t, int R128) {
+    if constexpr (SWZ) {
+        if constexpr (KIND == KIND_W8A8) {
+            const int c16 = 2 * c + (t >> 1);
+            return (c16 >> 3) * R128 + (((c16 & 7) ^ g) << 4) + 8 * (t & 1);
+        }
+        return (c >> 3) * R128 + (((c & 7) ^ g) << 4) + 4 * t;
+    } else {
+        return (KIND == KIND_W8A8) ? 32 * c + 8 * t : 16 * c + 4 * t;
+    }
+}
+
+// One unit (CPG chunks of 32 columns, starting at chunk c0 of the tile) of
+// one warp: MMA partial sums for the warp's 16-row block (rows g, g + 8 of
+// each thread) against MT 8-row activation tiles.  w0 / w8: rows g and g + 8
+// of the tile; xr[mt]: the thread's activations of the unit's first chunk.
+template <int KIND, bool SWZ, int RB, int MT, int CPG>
+W4_DEV void unit_mma(const uint8_t *w0, const uint8_t *w8, int c0, int g, int t, int R128,
+                     const uint8_t *const (&xr)[MT], const bool (&xvalid)[MT], int cpg_rt, float (&part)[MT][4]) {
+    const uint32_t xsel8[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
+    const int nc = CPG > 0 ? CPG : cpg_rt;
+#pragma unroll
+    for (int c = 0; c < (CPG > 0 ? CPG : 1); ++c) {
+        for (int cc = (CPG > 0 ? c : 0); cc < (CPG > 0 ? c + 1 : nc); ++cc) {
+            const int wo = wword_off<SWZ, KIND>(c0 + cc, g, t, R128);
+            uint32_t pa[4], pb[4] = {0u, 0u, 0u, 0u};
+            if constexpr (KIND == KIND_W4A16) {
+                unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w0 + wo), pa);
+                if (RB == 16) unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w8 + wo), pb);
+            } else if constexpr (KIND == KIND_W4A8) {
+                unpack_biased_f16(*reinterpret_cast<const uint32_t *>(w0 + wo), pa);
+                if (RB == 16) unpack_biased_f16(*reinterpret_cast<const uint32_t *>(w8 + wo), pb);
+            } else {
+                const uint2 wa = *reinterpret_cast<const uint2 *>(w0 + wo);
+                s8_to_f16_pairs(wa.x, wa.y, xsel8, pa);
+                if (RB == 16) {
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(w8 + wo);
+                    s8_to_f16_pairs(wb.x, wb.y, xsel8, pb);
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                // activations staged as f16/bf16 pairs in the order of the weight pairs
+                uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+                if (xvalid[mt]) xv = *reinterpret_cast<const uint4 *>(xr[mt] + 64 * cc);
+                if constexpr (KIND == KIND_W4A16) {
+                    mma_bf16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
+                    mma_bf16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+                } else {
+                    mma_f16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
+                    mma_f16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+//
+// One CTA: rows [row0, row0 + R) x the K range of split blockIdx.y.
+//  1. every thread issues 128-bit loads of its share of the weight tile and
+//     the W4A16 scales -- before the PDL wait, since no earlier kernel on the
+//     stream writes weights;
+//  2. griddepcontrol.wait, then 128-bit loads of the activation rows;
+//  3. the tiles go to shared memory (padded rows, conflict-free for the MMA
+//     fragment reads) and the CTA synchronises once;
+//  4. warps run the tensor-core k-reduction over their units, four units at
+//     a time with independent accumulators;
+//  5. K-split warps, then cluster ranks, are combined in index order.
+// A 32-column chunk is two m16n8k16 MMAs.  W4A16: bf16 operands (the signed
+// codes are exact bf16 integers), the group scale multiplies the f32
+// partial.  W4A8 / W8A8: f16 operands holding exact integers; each 32-column
+// unit's partial (|sum| <= 32 * 127 * 128 < 2^24) is exact in the f32
+// accumulator and is converted to i32 before it is added, so the integer
+// result is exact for any K.
+template <int KIND, bool N64, int RB, int MT, int CPG>
 __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
-    int *flag = reinterpret_cast<int *>(smem + p.flag_off);
-    int *xsum = reinterpret_cast<int *>(smem + p.xsum_off);
-
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wr = warp % p.WR, wk = warp / p.WR;
     const int g = lane >> 2, t = lane & 3;
@@ -121,150 +276,168 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     const int span_k = nun * p.unit_k;
     const int span_bytes = nun * p.unit_bytes;
     constexpr bool kInt = KIND != KIND_W4A16;
+    const int rows = min(p.R, p.N - row0);
+    const int nthr = blockDim.x;
 
-    if (tid == 0) {
-        mbar_init(bar, 1);
-        fence_mbar_init();
-        *flag = 1;
-    }
-    if (tid < 16) xsum[tid] = 0;
-    __syncthreads();
-
-    // ---- weight tile: bulk async copies, issued before the PDL wait.
-    if (tid == 0) {
-        if constexpr (!N64) {
-            const int rows = min(p.R, p.N - row0);
-            mbar_arrive_expect_tx(bar, (uint32_t)(rows * span_bytes));
-            const uint8_t *src = p.w + (size_t)row0 * p.Kb + (size_t)u0 * p.unit_bytes;
-            for (int r = 0; r < rows; ++r)
-                bulk_g2s(smem + p.w_off + r * p.wstride, src + (size_t)r * p.Kb, (uint32_t)span_bytes, bar);
-        } else {
-            const int kend = min(p.K, k0 + span_k);
-            const uint32_t bytes = (uint32_t)(kend - k0) * 32u;
-            mbar_arrive_expect_tx(bar, bytes);
-            bulk_g2s(smem + p.raw_off, p.w + ((size_t)blockIdx.x * p.K + k0) * 32, bytes, bar);
+    // ---- 1. weight-side loads into registers (16-byte vectors), issued
+    // before the PDL wait: no earlier kernel on the stream writes weights.
+    constexpr int kMaxLd = 8;  // 16-byte loads per thread per round
+    const int cpr = span_bytes >> 4;  // 16-byte chunks per row (row-major)
+    const uint32_t cpr_magic = div_magic((uint32_t)max(cpr, 1));
+    const int wchunks = N64 ? ((min(p.K, k0 + span_k) - k0) * 32) >> 4 : rows * cpr;
+    const uint8_t *wsrc = N64 ? p.w + ((size_t)blockIdx.x * p.K + k0) * 32
+                              : p.w + (size_t)row0 * p.Kb + (size_t)u0 * p.unit_bytes;
+    uint4 wv[kMaxLd];
+    {
+        const int lim = min(wchunks, kMaxLd * nthr);
+#pragma unroll
+        for (int i = 0; i < kMaxLd; ++i) {
+            const int j = tid + i * nthr;
+            if (j < lim) {
+                const uint8_t *src;
+                if constexpr (N64) src = wsrc + 16 * (size_t)j;
+                else {
+                    const int r = fast_div(j, cpr_magic);
+                    src = wsrc + (size_t)r * p.Kb + 16 * (j - r * cpr);
+                }
+                wv[i] = __ldg(reinterpret_cast<const uint4 *>(src));
+            }
         }
     }
-    // ---- W4A16 group scales (also weight-side data): f16 -> f32 into shared.
+    // W4A16 scales: 16-byte vectors when the rows allow it, converted to f32
+    // after the wait; otherwise a plain loop (odd shapes).
+    constexpr int kMaxSc = 2;
+    uint4 sv[kMaxSc];
+    const int spr = nun >> 3;  // 16-byte scale vectors per row
+    const bool svec = (KIND == KIND_W4A16) && p.s_vec && rows * spr <= kMaxSc * nthr;
+    const uint32_t spr_magic = div_magic((uint32_t)max(spr, 1));
     if constexpr (KIND == KIND_W4A16) {
-        float *sc = reinterpret_cast<float *>(smem + p.sc_off);
         const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
-        for (int i = tid; i < p.R * nun; i += blockDim.x) {
-            const int r = i / nun, gi = i - r * nun;
-            const int n = row0 + r;
-            sc[r * nun + gi] = n < p.N ? __half2float(__ushort_as_half(s16[(size_t)n * p.ng + u0 + gi])) : 0.0f;
+        if (svec) {
+#pragma unroll
+            for (int i = 0; i < kMaxSc; ++i) {
+                const int j = tid + i * nthr;
+                if (j < rows * spr) {
+                    const int r = fast_div(j, spr_magic);
+                    sv[i] = __ldg(reinterpret_cast<const uint4 *>(s16 + (size_t)(row0 + r) * p.ng + u0) + (j - r * spr));
+                }
+            }
+        } else {
+            const uint32_t nun_magic = div_magic((uint32_t)nun);
+            float *scf = reinterpret_cast<float *>(smem + p.sc_off);
+            for (int i = tid; i < rows * nun; i += nthr) {
+                const int r = fast_div(i, nun_magic), gi = i - r * nun;
+                scf[r * p.sstride + gi] = __half2float(__ushort_as_half(__ldg(s16 + (size_t)(row0 + r) * p.ng + u0 + gi)));
+            }
         }
     }
 
-    griddep_launch_dependents();
     griddep_wait();  // x may be written, and y read, by the previous kernel
 
-    // ---- activations: permuted copy of the CTA's K range, zero beyond K.
+    // ---- 2. activations: each group of 8 columns becomes four 16-bit pairs
+    // in the order of the weight pairs (zero beyond K):
+    //   W4A16 bf16 (x0 x4)(x1 x5)(x2 x6)(x3 x7); W4A8 the same as exact f16;
+    //   W8A8 f16 (x0 x1)(x2 x3)(x4 x5)(x6 x7).
     {
-        const int blocks8 = span_k >> 3;
-        const int jobs = p.M * blocks8;
-        for (int j = tid; j < jobs; j += blockDim.x) {
-            const int m = j / blocks8, b8 = j - m * blocks8;
+        const int per_row = span_k >> 3;  // 8-element groups
+        const uint32_t pr_magic = div_magic((uint32_t)per_row);
+        for (int j = tid; j < p.M * per_row; j += nthr) {
+            const int m = fast_div(j, pr_magic), b8 = j - m * per_row;
             const int kk = k0 + 8 * b8;
+            uint4 o;
             if constexpr (kInt) {
                 const int8_t *xr = static_cast<const int8_t *>(p.x) + (size_t)m * p.K;
-                uint32_t lo = 0, hi = 0;
+                uint2 v;
                 if (p.x_vec && kk + 8 <= p.K) {
-                    const uint2 v = *reinterpret_cast<const uint2 *>(xr + kk);
-                    lo = v.x;
-                    hi = v.y;
+                    v = __ldg(reinterpret_cast<const uint2 *>(xr + kk));
                 } else {
+                    uint32_t lo = 0, hi = 0;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const uint32_t b = (kk + i < p.K) ? (uint32_t)(uint8_t)xr[kk + i] : 0u;
                         if (i < 4) lo |= b << (8 * i);
                         else hi |= b << (8 * (i - 4));
                     }
+                    v = make_uint2(lo, hi);
                 }
-                uint8_t *dst = smem + p.x_off + m * p.xstride + 8 * b8;
-                if constexpr (KIND == KIND_W4A8) {
-                    // [x0 x2 x4 x6 | x1 x3 x5 x7]: bytes of the low/high nibble planes
-                    *reinterpret_cast<uint2 *>(dst) = make_uint2(prmt(lo, hi, 0x6420), prmt(lo, hi, 0x7531));
-                    int s = 0;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) s += (int)(int8_t)(lo >> (8 * i)) + (int)(int8_t)(hi >> (8 * i));
-                    atomicAdd(&xsum[m], s);
-                } else {
-                    *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
-                }
+                const uint32_t xsel4[4] = {0x0400u, 0x0501u, 0x0602u, 0x0703u};
+                const uint32_t xsel8[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
+                uint32_t b[4];
+                s8_to_f16_pairs(v.x, v.y, (KIND == KIND_W4A8) ? xsel4 : xsel8, b);
+                o = make_uint4(b[0], b[1], b[2], b[3]);
             } else {
                 const uint16_t *xr = static_cast<const uint16_t *>(p.x) + (size_t)m * p.K;
-                uint32_t i0 = 0, i1 = 0, i2 = 0, i3 = 0;
+                uint4 v;
                 if (p.x_vec && kk + 8 <= p.K) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(xr + kk);
-                    i0 = v.x; i1 = v.y; i2 = v.z; i3 = v.w;
+                    v = __ldg(reinterpret_cast<const uint4 *>(xr + kk));
                 } else {
                     uint32_t e[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) e[i] = (kk + i < p.K) ? (uint32_t)xr[kk + i] : 0u;
-                    i0 = e[0] | (e[1] << 16); i1 = e[2] | (e[3] << 16);
-                    i2 = e[4] | (e[5] << 16); i3 = e[6] | (e[7] << 16);
+                    v = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
                 }
-                // [x0 x4 | x1 x5 | x2 x6 | x3 x7] as bf16 pairs
-                uint4 o;
-                o.x = prmt(i0, i2, 0x5410);
-                o.y = prmt(i0, i2, 0x7632);
-                o.z = prmt(i1, i3, 0x5410);
-                o.w = prmt(i1, i3, 0x7632);
-                *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) = o;
+                o = make_uint4(prmt(v.x, v.z, 0x5410), prmt(v.x, v.z, 0x7632), prmt(v.y, v.w, 0x5410),
+                               prmt(v.y, v.w, 0x7632));
             }
+            *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) = o;
         }
     }
 
-    // ---- wait for the weight tile (bounded).
-    if (tid == 0) {
-        if (!mbar_wait_bounded(bar, 0)) {
-            atomicOr(p.status, kStatusCopyTimeout);
-            mbar_wait_bounded(bar, 0);  // give copies still in flight one more bounded chance
-            *flag = 0;
+    // ---- 3. weight tile into shared memory (further rounds for big tiles).
+    for (int base = 0; base < wchunks; base += kMaxLd * nthr) {
+        const int lim = min(wchunks - base, kMaxLd * nthr);
+        if (base > 0) {
+#pragma unroll
+            for (int i = 0; i < kMaxLd; ++i) {
+                const int j = base + tid + i * nthr;
+                if (tid + i * nthr < lim) {
+                    const uint8_t *src;
+                    if constexpr (N64) src = wsrc + 16 * (size_t)j;
+                    else {
+                        const int r = fast_div(j, cpr_magic);
+                        src = wsrc + (size_t)r * p.Kb + 16 * (j - r * cpr);
+                    }
+                    wv[i] = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kMaxLd; ++i) {
+            const int j = base + tid + i * nthr;
+            if (tid + i * nthr < lim) {
+                uint8_t *dst;
+                if constexpr (N64) dst = smem + p.raw_off + 16 * j;
+                else {
+                    const int r = fast_div(j, cpr_magic);
+                    dst = smem + p.w_off + r * p.wstride + 16 * (j - r * cpr);
+                }
+                *reinterpret_cast<uint4 *>(dst) = wv[i];
+            }
+        }
+    }
+    if constexpr (KIND == KIND_W4A16) {
+        if (svec) {
+            float *scf = reinterpret_cast<float *>(smem + p.sc_off);
+#pragma unroll
+            for (int i = 0; i < kMaxSc; ++i) {
+                const int j = tid + i * nthr;
+                if (j < rows * spr) {
+                    const int r = fast_div(j, spr_magic), c8 = j - r * spr;
+                    const uint32_t w4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        scf[r * p.sstride + 8 * c8 + e] =
+                            __half2float(__ushort_as_half((unsigned short)(w4[e >> 1] >> (16 * (e & 1)))));
+                }
+            }
         }
     }
     __syncthreads();
-    const bool ok = *flag != 0;
-    if (ok) mbar_wait_bounded(bar, 0);  // completed: acquire for every thread
+    // Let the next kernel on the stream start (and begin its weight fetch)
+    // once this CTA's tiles are in shared memory.
+    griddep_launch_dependents();
 
-    // ---- interleaved layout: transpose [k][32 B] into the row-major tile.
-    if constexpr (N64) {
-        if (ok) {
-            const uint8_t *raw = smem + p.raw_off;
-            const int jobs = (span_k >> 3) * 8;
-            for (int j = tid; j < jobs; j += blockDim.x) {
-                const int dq = j & 7, k8 = j >> 3;
-                uint32_t v[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint32_t *>(raw + (8 * k8 + i) * 32 + 4 * dq);
-                uint32_t T[2][4];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t a01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x5140);
-                    const uint32_t b01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x7362);
-                    const uint32_t a23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x5140);
-                    const uint32_t b23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x7362);
-                    T[h][0] = prmt(a01, a23, 0x5410);  // byte i = column 4h+i of channel 4dq+0
-                    T[h][1] = prmt(a01, a23, 0x7632);
-                    T[h][2] = prmt(b01, b23, 0x5410);
-                    T[h][3] = prmt(b01, b23, 0x7632);
-                }
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t la = T[0][c] & 0x0F0F0F0Fu, lb = T[1][c] & 0x0F0F0F0Fu;
-                    const uint32_t ha = (T[0][c] >> 4) & 0x0F0F0F0Fu, hb = (T[1][c] >> 4) & 0x0F0F0F0Fu;
-                    const uint32_t lo = prmt(la | (la >> 4), lb | (lb >> 4), 0x6420);
-                    const uint32_t hi = prmt(ha | (ha >> 4), hb | (hb >> 4), 0x6420);
-                    *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c) * p.wstride + 4 * k8) = lo;
-                    *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c + 32) * p.wstride + 4 * k8) = hi;
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    // ---- tensor-core k-reduction.
+    // ---- 4. tensor-core k-reduction.
     using Acc = typename std::conditional<kInt, int, float>::type;
     Acc acc[MT][4];
 #pragma unroll
@@ -273,80 +446,98 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
         for (int i = 0; i < 4; ++i) acc[mt][i] = 0;
 
     const int rbase = wr * RB;
-    if (ok) {
-        constexpr int kWordBytes = (KIND == KIND_W8A8) ? 8 : 4;
-        const uint8_t *wrow = smem + p.w_off + (rbase + g) * p.wstride + kWordBytes * t;
-        const uint8_t *wrow8 = wrow + 8 * p.wstride;
-        const uint8_t *xrow[MT];
-        bool xvalid[MT];
+    const int cpg = CPG > 0 ? CPG : p.cpg;
+    const int R128 = p.R * 128;
+    const uint8_t *wrow = smem + p.w_off + (rbase + g) * p.wstride;
+    const uint8_t *wrow8 = wrow + 8 * p.wstride;
+    const uint8_t *xrow[MT];
+    bool xvalid[MT];
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            const int m = g + 8 * mt;
-            xvalid[mt] = m < p.M;
-            xrow[mt] = smem + p.x_off + (xvalid[mt] ? m : 0) * p.xstride + (kInt ? 8 : 16) * t;
+    for (int mt = 0; mt < MT; ++mt) {
+        const int m = g + 8 * mt;
+        xvalid[mt] = m < p.M;
+        xrow[mt] = smem + p.x_off + (xvalid[mt] ? m : 0) * p.xstride + 16 * t;
+    }
+    const float *scf = reinterpret_cast<const float *>(smem + p.sc_off);
+    const float *sc0 = scf + (rbase + g) * p.sstride;
+    const float *sc1 = scf + (rbase + g + 8) * p.sstride;
+
+    // fold one unit's partial into acc (units arrive in increasing order)
+    auto fold = [&](const float (&part)[MT][4], int u) {
+        if constexpr (KIND == KIND_W4A16) {
+            const float s0 = sc0[u];
+            const float s1 = (RB == 16) ? sc1[u] : 0.0f;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                acc[mt][0] = fmaf(s0, part[mt][0], acc[mt][0]);
+                acc[mt][1] = fmaf(s0, part[mt][1], acc[mt][1]);
+                acc[mt][2] = fmaf(s1, part[mt][2], acc[mt][2]);
+                acc[mt][3] = fmaf(s1, part[mt][3], acc[mt][3]);
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[mt][i] += __float2int_rn(part[mt][i]);
         }
-        for (int u = wk; u < nun; u += p.WK) {
-            if constexpr (KIND == KIND_W4A16) {
-                float part[MT][4];
+    };
+    auto run_unit = [&](int u, int ul, float (&part)[MT][4]) {
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
+        for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) part[mt][i] = 0.0f;
-                for (int c = 0; c < p.cpg; ++c) {
-                    const int chunk = u * p.cpg + c;
-                    uint32_t pa[4], pb[4] = {0u, 0u, 0u, 0u};
-                    unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(wrow + 16 * chunk), pa);
-                    if (RB == 16) unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(wrow8 + 16 * chunk), pb);
+            for (int i = 0; i < 4; ++i) part[mt][i] = 0.0f;
+        const uint8_t *xr[MT];
 #pragma unroll
-                    for (int mt = 0; mt < MT; ++mt) {
-                        uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-                        if (xvalid[mt]) xv = *reinterpret_cast<const uint4 *>(xrow[mt] + 64 * chunk);
-                        mma_bf16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
-                        mma_bf16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
-                    }
-                }
-                const float *sc = reinterpret_cast<const float *>(smem + p.sc_off);
-                const float s0 = sc[(rbase + g) * nun + u];
-                const float s1 = (RB == 16) ? sc[(rbase + g + 8) * nun + u] : 0.0f;
+        for (int mt = 0; mt < MT; ++mt) xr[mt] = xrow[mt] + 64 * cpg * u;
+        unit_mma<KIND, false, RB, MT, CPG>(wrow, wrow8, cpg * ul, g, t, R128, xr, xvalid, cpg, part);
+    };
+
+    // Units are processed in phases (one phase for the row-major layout); a
+    // warp always takes units wk, wk + WK, ... in increasing order, so both
+    // layouts accumulate every output in the same order.
+    const int upp = N64 ? p.upp : nun;
+    const int WK = p.WK;
+    for (int ph0 = 0; ph0 < nun; ph0 += upp) {
+        const int ph1 = min(nun, ph0 + upp);
+        const int wbase = N64 ? ph0 : 0;  // unit index of the tile's first unit
+        if constexpr (N64) {
+            // transpose this phase's columns into the row-major tile
+            const int kq = (ph1 - ph0) * p.unit_k / 8;  // 8-column groups in the phase
+            const uint8_t *raw = smem + p.raw_off + (size_t)ph0 * p.unit_k * 32;
+            for (int j = tid; j < kq * 8; j += nthr) {
+                const int dq = j & 7, k8 = j >> 3;
+                uint32_t lo[4], hi[4];
+                deinterleave8(raw + k8 * 8 * 32, dq, lo, hi);
 #pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    acc[mt][0] = fmaf(s0, part[mt][0], acc[mt][0]);
-                    acc[mt][1] = fmaf(s0, part[mt][1], acc[mt][1]);
-                    acc[mt][2] = fmaf(s1, part[mt][2], acc[mt][2]);
-                    acc[mt][3] = fmaf(s1, part[mt][3], acc[mt][3]);
-                }
-            } else if constexpr (KIND == KIND_W4A8) {
-                const int chunk = u;
-                const uint32_t wa = *reinterpret_cast<const uint32_t *>(wrow + 16 * chunk);
-                const uint32_t wb = (RB == 16) ? *reinterpret_cast<const uint32_t *>(wrow8 + 16 * chunk) : 0u;
-                // biased codes u in [0, 15] are non-negative int8 values
-                const uint32_t a0 = wa & 0x0F0F0F0Fu, a2 = (wa >> 4) & 0x0F0F0F0Fu;
-                const uint32_t a1 = wb & 0x0F0F0F0Fu, a3 = (wb >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    uint2 xv = make_uint2(0u, 0u);
-                    if (xvalid[mt]) xv = *reinterpret_cast<const uint2 *>(xrow[mt] + 32 * chunk);
-                    mma_s8(acc[mt], a0, a1, a2, a3, xv.x, xv.y);
-                }
-            } else {  // W8A8
-                const int chunk = u;
-                const uint2 wa = *reinterpret_cast<const uint2 *>(wrow + 32 * chunk);
-                uint2 wb = make_uint2(0u, 0u);
-                if (RB == 16) wb = *reinterpret_cast<const uint2 *>(wrow8 + 32 * chunk);
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt) {
-                    uint2 xv = make_uint2(0u, 0u);
-                    if (xvalid[mt]) xv = *reinterpret_cast<const uint2 *>(xrow[mt] + 32 * chunk);
-                    mma_s8(acc[mt], wa.x, wb.x, wa.y, wb.y, xv.x, xv.y);
+                for (int c = 0; c < 4; ++c) {
+                    *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c) * p.wstride + 4 * k8) = lo[c];
+                    *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c + 32) * p.wstride + 4 * k8) = hi[c];
                 }
             }
+            __syncthreads();
         }
+        // four units at a time, each with its own partial accumulators so the
+        // MMA chains overlap, then the remaining units one by one
+        int u = ph0 + wk;
+        for (; u + 3 * WK < ph1; u += 4 * WK) {
+            float part[4][MT][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) run_unit(u + j * WK, u + j * WK - wbase, part[j]);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) fold(part[j], u + j * WK);
+        }
+        for (; u < ph1; u += WK) {
+            float part[MT][4];
+            run_unit(u, u - wbase, part);
+            fold(part, u);
+        }
+        if constexpr (N64) __syncthreads();  // the next phase overwrites the tile
     }
 
-    // ---- combine the K-split warps in index order.
+    // ---- 5. combine the K-split warps in index order.
     uint32_t *red = reinterpret_cast<uint32_t *>(smem + p.red_off);
     constexpr int kVals = MT * 4;
-    if (p.WK > 1) {
+    if (WK > 1) {
         if (wk > 0) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
@@ -357,7 +548,7 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
         }
         __syncthreads();
         if (wk == 0) {
-            for (int w2 = 1; w2 < p.WK; ++w2)
+            for (int w2 = 1; w2 < WK; ++w2)
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -368,20 +559,9 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
                     }
         }
     }
-    // W4A8: this CTA's share of the bias correction, -8 * sum of its x columns.
-    if constexpr (KIND == KIND_W4A8) {
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int m = 8 * mt + 2 * t + (i & 1);
-                if (m < p.M) acc[mt][i] -= 8 * xsum[m];
-            }
-    }
 
     // ---- combine the cluster's K splits in rank order (distributed shared memory).
     const int S = gridDim.y;
-    bool all_ok = ok;
     if (S > 1) {
         __syncthreads();  // red is reused below
         if (wk == 0) {
@@ -395,7 +575,6 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
         cluster_sync();
         if (blockIdx.y == 0 && wk == 0) {
             for (int r = 1; r < S; ++r) {
-                all_ok = all_ok && dsmem_ld_u32(dsmem_map(flag, (uint32_t)r)) != 0;
 #pragma unroll
                 for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -411,7 +590,7 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     }
 
     // ---- epilogue.
-    if (blockIdx.y != 0 || wk != 0 || !all_ok) return;
+    if (blockIdx.y != 0 || wk != 0) return;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
@@ -490,12 +669,12 @@ struct Shape {
     int RB, WR, WK, S, MT;
 };
 
-template <int KIND, bool N64, int RB, int MT>
+template <int KIND, bool N64, int RB, int MT, int CPG>
 cudaError_t launch_one(const GemvParams &p, int S, int threads, int smem, cudaStream_t st, bool pdl) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<KIND, N64, RB, MT>,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<KIND, N64, RB, MT, CPG>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -520,21 +699,30 @@ cudaError_t launch_one(const GemvParams &p, int S, int threads, int smem, cudaSt
     }
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, N64, RB, MT>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, N64, RB, MT, CPG>, p);
 }
 
-template <int KIND, bool N64>
+template <int KIND, bool N64, int CPG>
 cudaError_t dispatch_rb_mt(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
     if (s.RB == 8) {
-        if (s.MT == 1) return launch_one<KIND, N64, 8, 1>(p, s.S, threads, smem, st, pdl);
-        return launch_one<KIND, N64, 8, 2>(p, s.S, threads, smem, st, pdl);
+        if (s.MT == 1) return launch_one<KIND, N64, 8, 1, CPG>(p, s.S, threads, smem, st, pdl);
+        return launch_one<KIND, N64, 8, 2, CPG>(p, s.S, threads, smem, st, pdl);
     }
-    if (s.MT == 1) return launch_one<KIND, N64, 16, 1>(p, s.S, threads, smem, st, pdl);
-    return launch_one<KIND, N64, 16, 2>(p, s.S, threads, smem, st, pdl);
+    if (s.MT == 1) return launch_one<KIND, N64, 16, 1, CPG>(p, s.S, threads, smem, st, pdl);
+    return launch_one<KIND, N64, 16, 2, CPG>(p, s.S, threads, smem, st, pdl);
 }
 
-constexpr int kTargetCtas = 2 * 152;
+template <bool N64>
+cudaError_t dispatch_w4a16(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
+    switch (p.cpg) {
+        case 1: return dispatch_rb_mt<KIND_W4A16, N64, 1>(p, s, threads, smem, st, pdl);
+        case 4: return dispatch_rb_mt<KIND_W4A16, N64, 4>(p, s, threads, smem, st, pdl);
+        default: return dispatch_rb_mt<KIND_W4A16, N64, 0>(p, s, threads, smem, st, pdl);
+    }
+}
+
 constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMinTiles = 128;  // CTAs (of 8 rows) below which K is split across a cluster
 
 // Fills the unit geometry of p for the call; false when the fast path cannot describe it.
 bool geometry(const LinearArgs &a, GemvParams &p) {
@@ -554,23 +742,20 @@ bool geometry(const LinearArgs &a, GemvParams &p) {
     return true;
 }
 
-// Shared-memory carve-up for a given shape; returns total bytes.
+int pad_to(int bytes, int target) { return bytes + ((target - bytes % 128) + 256) % 128; }
+
+// Shared-memory carve-up for a given shape (p.upc, p.upp set); returns total bytes.
 int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p) {
     const bool n64 = a.layout == W4_LAYOUT_N64;
     p.R = n64 ? 64 : s.RB * s.WR;
     p.WR = n64 ? 64 / s.RB : s.WR;
     p.WK = s.WK;
     const int span_k = p.upc * p.unit_k;
-    const int span_bytes = p.upc * p.unit_bytes;
-    const int wtarget = (a.kind == KIND_W8A8) ? 32 : 16;
-    p.wstride = span_bytes + ((wtarget - span_bytes % 128) + 256) % 128;
-    const int esize = (a.kind == KIND_W4A16) ? 2 : 1;
-    const int xtarget = (a.kind == KIND_W4A16) ? 64 : 32;
-    const int xbytes = span_k * esize;
-    p.xstride = xbytes + ((xtarget - xbytes % 128) + 256) % 128;
-    int off = 128;  // mbarrier + flag live in the first 128 bytes
-    p.flag_off = 16;
-    p.xsum_off = 64;
+    const int tile_units = n64 ? p.upp : p.upc;
+    p.wstride = pad_to(tile_units * p.unit_bytes, (a.kind == KIND_W8A8) ? 32 : 16);
+    p.xstride = pad_to(span_k * 2, 64);  // staged as 16-bit pairs for every kind
+    p.sstride = p.upc | 1;  // f32 scales per row, odd so the 8 rows of a warp hit 8 banks
+    int off = 0;
     p.raw_off = off;
     if (n64) off += (int)round_up((int64_t)span_k * 32, 128);
     p.w_off = off;
@@ -578,7 +763,7 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p) {
     p.x_off = off;
     off += (int)round_up((int64_t)a.M * p.xstride, 128);
     p.sc_off = off;
-    if (a.kind == KIND_W4A16) off += (int)round_up((int64_t)p.R * p.upc * 4, 128);
+    if (a.kind == KIND_W4A16) off += (int)round_up((int64_t)p.R * p.sstride * 4, 128);
     p.red_off = off;
     const int warps = p.WR * p.WK;
     off += (int)round_up((int64_t)warps * 32 * ((a.M > 8) ? 8 : 4) * 4, 128);
@@ -589,7 +774,7 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p) {
 
 bool gemv_supported(const LinearArgs &a) {
     if (a.M > 16 || a.M < 1) return false;
-    if (a.N > 0x7FFFFFFF / 2 || a.K > 0x7FFFFFF) return false;
+    if (a.N > 0x3FFFFFFF || a.K > 0x7FFFFFF) return false;
     if (a.kind == KIND_W8A8 && a.layout != W4_LAYOUT_ROWMAJOR) return false;
     GemvParams p = {};
     if (!geometry(a, p)) return false;
@@ -610,7 +795,6 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     p.N = (int)a.N;
     p.K = (int)a.K;
     const int esize = (a.kind == KIND_W4A16) ? 2 : 1;
-    p.x_vec = ((a.K * esize) % 16 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) ? 1 : 0;
     const bool n64 = a.layout == W4_LAYOUT_N64;
 
     // The K split (warps per CTA along K, cluster ranks along K) depends only
@@ -619,47 +803,62 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     Shape s;
     s.MT = a.M > 8 ? 2 : 1;
     s.WK = std::max(1, std::min(4, p.units));
-    int S = (int)std::min<int64_t>(8, ceil_div(kTargetCtas, ceil_div(a.N, 8)));
+    const int64_t tiles8 = ceil_div(a.N, 8);
+    int S = tiles8 >= kMinTiles ? 1 : (int)std::min<int64_t>(8, ceil_div(kMinTiles, tiles8));
     S = std::max(1, std::min(S, p.units / s.WK));
+    // units per interleave phase: ~512 packed bytes per row, a multiple of WK
+    p.upp = std::max(s.WK, (512 / p.unit_bytes) / s.WK * s.WK);
+    // A split starts on a 128-byte column boundary: units per split are a
+    // multiple of lcm(unit, 128) / unit.
+    const int ualign = std::lcm(p.unit_bytes, 128) / p.unit_bytes;
     {
-        LinearArgs worst = a;  // size the split for the largest tile any M or layout uses
+        // size the split for the largest tile any M or layout uses
+        LinearArgs worst = a;
         worst.M = 16;
-        worst.layout = W4_LAYOUT_N64;
         Shape sw = s;
         sw.RB = 16;
         sw.WR = 4;
         GemvParams q = p;
         for (;;) {
-            q.upc = (int)ceil_div(p.units, S);
+            q.upc = (int)round_up(ceil_div(p.units, S), ualign);
             S = (int)ceil_div(p.units, q.upc);  // no empty splits
-            if (plan_smem(worst, sw, q) <= kSmemLimit || S >= 8 || S >= p.units) break;
+            worst.layout = W4_LAYOUT_N64;
+            const int a1 = plan_smem(worst, sw, q);
+            worst.layout = W4_LAYOUT_ROWMAJOR;
+            const int a2 = plan_smem(worst, sw, q);
+            if (std::max(a1, a2) <= kSmemLimit || S >= 8 || q.upc <= ualign) break;
             ++S;
         }
     }
-    p.upc = (int)ceil_div(p.units, S);
+    p.upc = (int)round_up(ceil_div(p.units, S), ualign);
+    S = (int)ceil_div(p.units, p.upc);
     if (n64) {
         s.RB = 16;
         s.WR = 4;
     } else {
-        s.RB = (a.N >= 16 * kTargetCtas || a.M > 4) ? 16 : 8;
+        s.RB = (a.N >= 16 * 2 * 152 || a.M > 4) ? 16 : 8;
         s.WR = 1;
         if (a.M >= 4)
-            while (s.WR < 4 && a.N / (s.RB * s.WR * 2) >= kTargetCtas) s.WR *= 2;
+            while (s.WR < 4 && a.N / (s.RB * s.WR * 2) >= 2 * 152) s.WR *= 2;
     }
     const int smem = plan_smem(a, s, p);
     if (smem > kSmemLimit) return launch_generic(a, st);
+
+    p.x_vec = ((a.K * esize) % 16 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) ? 1 : 0;
+    p.s_vec = (a.kind == KIND_W4A16 && p.ng % 8 == 0 && p.upc % 8 == 0 &&
+               reinterpret_cast<uintptr_t>(a.scale) % 16 == 0) ? 1 : 0;
     s.S = S;
     const int threads = 32 * p.WR * p.WK;
     const bool pdl = (a.flags & W4_FLAG_PDL) != 0;
     switch (a.kind) {
         case KIND_W4A8:
-            return n64 ? dispatch_rb_mt<KIND_W4A8, true>(p, s, threads, smem, st, pdl)
-                       : dispatch_rb_mt<KIND_W4A8, false>(p, s, threads, smem, st, pdl);
+            return n64 ? dispatch_rb_mt<KIND_W4A8, true, 1>(p, s, threads, smem, st, pdl)
+                       : dispatch_rb_mt<KIND_W4A8, false, 1>(p, s, threads, smem, st, pdl);
         case KIND_W8A8:
-            return dispatch_rb_mt<KIND_W8A8, false>(p, s, threads, smem, st, pdl);
+            return dispatch_rb_mt<KIND_W8A8, false, 1>(p, s, threads, smem, st, pdl);
         default:
-            return n64 ? dispatch_rb_mt<KIND_W4A16, true>(p, s, threads, smem, st, pdl)
-                       : dispatch_rb_mt<KIND_W4A16, false>(p, s, threads, smem, st, pdl);
+            return n64 ? dispatch_w4a16<true>(p, s, threads, smem, st, pdl)
+                       : dispatch_w4a16<false>(p, s, threads, smem, st, pdl);
     }
 }
 

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace w4 {
@@ -25,6 +26,10 @@ struct LinearArgs {
     size_t ws_bytes;
     uint32_t *status;    // device status word
 };
+
+// tmap.cu -- TMA tensor map of a tiled box (rank <= 5); strides of dims 1..rank-1 in bytes.
+bool encode_tmap(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
 // quant.cu
 cudaError_t launch_quantize_rows(const float *x, int64_t rows, int64_t K, int Q, int8_t *q, float *s,
