@@ -340,6 +340,49 @@ def time_e2e(w, steps: int):
             "ms_per_step": ms / steps}
 
 
+def prefill_lines(peaks):
+    """W4A8 / W4A16 prefill (M = 2048, K = 2048, N in {2048, 3072, 13312}): ops/s of the tensor path."""
+    import torch
+    from w4a16_int4_quantized_gb300 import ops, synth
+    out = []
+    M, K, G = 2048, 2048, 128
+    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    for N in (2048, 3072, 13312):
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        x, W = synth.w4a8_inputs(1005, M, N, K)
+        xq, sx, _ = ops.quantize_row_q8(dev(x))
+        wq, sw = ops.quantize_matrix_q4(dev(W))
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        ws = torch.empty(ops.workspace_bytes(ops.OP_LINEAR_Q4, M, N, K), dtype=torch.uint8, device="cuda")
+        xb, wb, sb = synth.w4a16_inputs(1006, M, N, K, G)
+        xbd, wbd, sbd = dev(xb), dev(wb), dev(sb)
+        runs = {
+            "w4a8": lambda: ops.linear_q4(xq, sx, wq, sw, K=K, out=y, workspace=ws),
+            "w4a16": lambda: ops.linear_w4a16_group(xbd, wbd, sbd, G, K=K, out=y),
+        }
+        for name, fn in runs.items():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            reps = 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                fn()
+            e1.record()
+            e1.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            tops = 2.0 * M * N * K / (ms / 1e3) / 1e12
+            out.append({"workload": f"{name}_prefill_m{M}_n{N}_k{K}", "metric": "TOPS" if name == "w4a8" else "TFLOP/s",
+                        "value": round(tops, 1), "ms_per_call": round(ms, 4),
+                        "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
+                                     "frac": round(tops / bf16_peak, 4),
+                                     "note": "f16/bf16 tcgen05 path; peak = measured bf16 dense (f16 same rate)"}})
+        del xq, wq, y, ws, xbd, wbd, sbd
+        torch.cuda.empty_cache()
+    return out
+
+
 def extra_lines(l2: int, peak_gbs: float):
     import torch
     out = []
@@ -440,7 +483,7 @@ def run_ours(args, world, rank, local):
     cpu = None
     if not args.no_cpu:
         cpu, _, _ = time_oracle(w, args.cpu_seconds)
-    extra = [] if args.no_extra else extra_lines(l2, peak)
+    extra = [] if args.no_extra else extra_lines(l2, peak) + prefill_lines(peaks)
     line = {
         "metric": "int4 linear weight GB/s (M=1 decode)",
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

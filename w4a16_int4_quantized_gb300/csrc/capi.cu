@@ -7,6 +7,7 @@
 // is no CPU fallback: every result comes from a kernel.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -64,6 +65,25 @@ w4_status run_linear(w4::LinearArgs &a, cudaStream_t st) {
     a.status = status;
     if (a.M <= 16 && w4::gemv_supported(a)) return cuda_status(w4::launch_gemv(a, st));
     if (a.M > 16 && w4::gemm_supported(a)) return cuda_status(w4::launch_gemm(a, st));
+    // M > 16 shapes the tensor-core GEMM does not take (interleaved layout,
+    // odd K, W8A8 with K > 1024): slices of 16 activation rows through the
+    // decode kernel, which handles them exactly.
+    w4::LinearArgs s16 = a;
+    s16.M = 16;
+    if (a.M > 16 && w4::gemv_supported(s16)) {
+        const size_t xrow = (size_t)a.K * (a.kind == w4::KIND_W4A16 ? 2 : 1);
+        for (int64_t m0 = 0; m0 < a.M; m0 += 16) {
+            w4::LinearArgs sl = a;
+            sl.M = std::min<int64_t>(16, a.M - m0);
+            sl.x = static_cast<const uint8_t *>(a.x) + (size_t)m0 * xrow;
+            sl.sx = a.sx ? a.sx + m0 : nullptr;
+            sl.y = a.y + (size_t)m0 * a.N;
+            sl.flags = 0;
+            const cudaError_t e = w4::launch_gemv(sl, st);
+            if (e != cudaSuccess) return cuda_status(e);
+        }
+        return W4_OK;
+    }
     return cuda_status(w4::launch_generic(a, st));
 }
 

@@ -1,12 +1,486 @@
-// gemm_tc.cu -- prefill (M > 16) tensor-core GEMM.  Filled in by the tcgen05 path.
+// gemm_tc.cu -- prefill linears (M > 16) on the 5th-generation tensor cores.
+//
+// y[m][n] = sum_k x[m][k] W[n][k], W never stored in float in global memory.
+//
+// Per CTA: a 128 (output channels n) x 256 (activation rows m) tile of y,
+// accumulated in tensor memory over K in steps of 64 columns:
+//   warp 0      TMA producer: the packed weight tile [128 rows][32|64 B] and
+//               the 16-bit activation tile [256 rows][64] (128-byte swizzle)
+//               of each stage, both on one transaction-count mbarrier;
+//   warp 1      allocates 256 TMEM columns and issues tcgen05.mma (one
+//               thread): kind::f16, A = weights (M = 128), B = activations
+//               (N = 256), K-major shared-memory descriptors, f32 accumulator;
+//               tcgen05.commit releases each stage and finally the tile;
+//   warps 2-9   convert the packed weights of a stage into the A operand tile
+//               (128B-swizzled, K-major) and later run the epilogue:
+//               tcgen05.ld of the accumulator, scales, coalesced stores.
+// Weight conversion (the dequantisation happens only in shared memory):
+//   W4A16  w = bf16_rne(f32(q) * f32(s)): q * s is exact in f32 and rounded
+//          once to bf16 ("Fused int4 ..." sections 2.2-2.3 dequantised once per
+//          tile, as vllm-omni "The 4-bit CPU path" does for large batches);
+//   W4A8   f16(q), q = u - 8 in [-8, 7]: exact;
+//   W8A8   f16(q), q in [-128, 127]: exact.
+// For the integer kinds the activations are the exact f16 images of the int8
+// codes, every product is an exact integer and every partial sum an integer
+// of magnitude <= 127 * max|q| * K, below 2^24 for W4A8 (|q| <= 8) up to
+// K = 16384 and for W8A8 (|q| <= 128) up to K = 1024 -- the shapes this path
+// accepts -- so the f32 accumulator holds the exact i32 dot product; the
+// epilogue applies y = (f32(acc) * sx[m]) * sw[n] like the decode path.
+//
+// Every mbarrier wait is bounded (about one second of %globaltimer); a wait
+// that runs out sets the status word, raises a CTA-wide abort flag that ends
+// every other wait at once, and the tile is not stored.  TMEM is always
+// released before the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
 #include "internal.h"
+#include "w4.h"
 
 namespace w4 {
+namespace {
 
-bool gemm_supported(const LinearArgs &) { return false; }
+constexpr int kBM = 128;   // weight rows per tile (UMMA M)
+constexpr int kBN = 256;   // activation rows per tile (UMMA N)
+constexpr int kBK = 64;    // columns per stage (128 bytes of 16-bit values)
+constexpr int kStages = 4;
+constexpr int kConvWarps = 8;
+constexpr int kThreads = 64 + 32 * kConvWarps;
+constexpr int kTmemCols = 256;
 
-size_t gemm_workspace_bytes(int, int64_t, int64_t, int64_t, int64_t) { return 0; }
+struct GemmParams {
+    CUtensorMap xmap;  // 16-bit activations [M][Kx], box {64, 256}, 128B swizzle
+    CUtensorMap wmap;  // packed weights [N][Kb] bytes, box {32|64, 128}
+    const uint16_t *scales;  // W4A16: f16 [N][ng]
+    const float *sx;         // int kinds: [M]
+    const float *sw;         // int kinds: [N]
+    float *y;                // [M][N]
+    uint32_t *status;
+    int M, N, K, G, ng;
+    int nk;  // k-blocks of 64 columns
+};
 
-cudaError_t launch_gemm(const LinearArgs &, cudaStream_t) { return cudaErrorNotSupported; }
+struct Smem {
+    uint64_t tma_full[kStages];
+    uint64_t conv_full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// ---------------------------------------------------------------- tcgen05 wrappers
+
+W4_DEV void tmem_alloc(uint32_t *dst_smem, uint32_t cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+W4_DEV void tmem_dealloc(uint32_t taddr, uint32_t cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(cols) : "memory");
+}
+W4_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+W4_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor, K-major operand, 128-byte swizzle:
+// 8-row atoms of 1024 bytes (stride byte offset 1024), start address >> 4.
+W4_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset: next 8-row atom
+    d |= (uint64_t)1 << 46;             // descriptor version
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, A/B f16 (0) or bf16 (1),
+// both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_fmt, uint32_t M, uint32_t N) {
+    return (1u << 4) | (ab_fmt << 7) | (ab_fmt << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+W4_DEV void umma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+W4_DEV void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 32 consecutive accumulator columns of the warp's 32 TMEM lanes.
+W4_DEV void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Bounded wait that also ends as soon as another role has aborted.
+W4_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, Smem *sh, uint32_t *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*reinterpret_cast<volatile int *>(&sh->abort)) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusPipeTimeout);
+            *reinterpret_cast<volatile int *>(&sh->abort) = 1;
+            return false;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- weight conversion
+
+// 8 packed signed nibbles (columns c..c+7) -> 8 bf16 = bf16_rne(q * s), as 16 bytes.
+W4_DEV uint4 conv_w4a16(uint32_t w, float s) {
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = (w >> (8 * e)) & 0xFu, hi = (w >> (8 * e + 4)) & 0xFu;
+        // 2^23 + (u ^ 8) = 2^23 + 8 + q exactly; subtracting 2^23 + 8 leaves q
+        const float ql = __int_as_float(0x4B000000 | (lo ^ 8u)) - 8388616.0f;
+        const float qh = __int_as_float(0x4B000000 | (hi ^ 8u)) - 8388616.0f;
+        __nv_bfloat162 b = __floats2bfloat162_rn(ql * s, qh * s);
+        o[e] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8 packed biased nibbles -> 8 f16 of q = u - 8 (exact), natural column order.
+W4_DEV uint4 conv_w4a8(uint32_t w) {
+    const __half2 mul = __halves2half2(__float2half(1.0f), __float2half(0.0625f));
+    const __half2 add = __halves2half2(__float2half(-1032.0f), __float2half(-72.0f));
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        // byte e in both halves: low half 0x6400 | lo = 1024 + lo, high half 0x6400 | (hi << 4) = 1024 + 16 hi
+        const uint32_t t = prmt(w, 0u, 0x4040u | ((uint32_t)e * 0x0101u));
+        const uint32_t v = (t & 0x00F0000Fu) | 0x64006400u;
+        __half2 h = __hfma2(*reinterpret_cast<const __half2 *>(&v), mul, add);
+        o[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 8 int8 (two words) -> 8 f16 of the same integers, natural order.
+W4_DEV uint4 conv_w8a8(uint32_t lo, uint32_t hi) {
+    const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6480), __ushort_as_half((unsigned short)0x6480));
+    lo ^= 0x80808080u;
+    hi ^= 0x80808080u;
+    const uint32_t sel[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t v = (prmt(lo, hi, sel[e]) & 0x00FF00FFu) | 0x64006400u;
+        __half2 h = __hsub2(*reinterpret_cast<const __half2 *>(&v), off);
+        o[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+    constexpr bool kW4 = KIND != KIND_W8A8;
+    constexpr int kPRow = kW4 ? 32 : 64;             // packed bytes per weight row per stage
+    constexpr int kATile = kBM * 128;                // 16 KB
+    constexpr int kBTile = kBN * 128;                // 32 KB
+    constexpr int kPTile = kBM * kPRow;              // 4 | 8 KB
+    constexpr uint32_t kStageTx = kBTile + kPTile;
+    constexpr uint32_t kIdesc = idesc_f16(KIND == KIND_W4A16 ? 1u : 0u, kBM, kBN);
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Smem *sh = reinterpret_cast<Smem *>(smem);
+    uint8_t *a_tiles = smem + 1024;
+    uint8_t *b_tiles = a_tiles + kStages * kATile;
+    uint8_t *p_tiles = b_tiles + kStages * kBTile;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * kBN;  // activation rows
+    const int n0 = blockIdx.y * kBM;  // weight rows
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sh->tma_full[s], 1);
+            mbar_init(&sh->conv_full[s], 32 * kConvWarps);
+            mbar_init(&sh->empty[s], 1);
+        }
+        mbar_init(&sh->acc_full, 1);
+        sh->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&sh->tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    if (warp == 0) {
+        // ---------------- TMA producer
+        if (lane == 0) {
+            for (int kb = 0; kb < p.nk; ++kb) {
+                const int s = kb % kStages;
+                if (kb >= kStages && !wait_or_abort(&sh->empty[s], ((kb / kStages) - 1) & 1, sh, p.status)) break;
+                mbar_arrive_expect_tx(&sh->tma_full[s], kStageTx);
+                tma_load_2d(b_tiles + s * kBTile, &p.xmap, kb * kBK, m0, &sh->tma_full[s]);
+                tma_load_2d(p_tiles + s * kPTile, &p.wmap, kb * kPRow, n0, &sh->tma_full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            bool ok = true;
+            for (int kb = 0; kb < p.nk && ok; ++kb) {
+                const int s = kb % kStages;
+                const uint32_t ph = (kb / kStages) & 1;
+                ok = wait_or_abort(&sh->tma_full[s], ph, sh, p.status) &&
+                     wait_or_abort(&sh->conv_full[s], ph, sh, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(a_tiles + s * kATile);
+                const uint32_t b_addr = smem_u32(b_tiles + s * kBTile);
+#pragma unroll
+                for (int j = 0; j < kBK / 16; ++j)  // 16 columns (32 bytes) per MMA
+                    umma_f16(tmem, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), kIdesc,
+                             (kb > 0 || j > 0) ? 1u : 0u);
+                umma_commit(&sh->empty[s]);
+            }
+            if (ok) umma_commit(&sh->acc_full);
+        }
+    } else {
+        // ---------------- weight conversion (warps 2..9: 256 threads)
+        const int ct = tid - 64;
+        const int row = ct & (kBM - 1), half = ct >> 7;  // row of the tile, columns [32 half, 32 half + 32)
+        const int n = n0 + row;
+        const int rr = row & 7;
+        uint8_t *a_row = a_tiles + (row >> 3) * 1024 + rr * 128;
+        // W4A16 group scales of this thread's 4 chunks, fetched one stage ahead
+        float sc_cur[4] = {0.f, 0.f, 0.f, 0.f}, sc_nxt[4] = {0.f, 0.f, 0.f, 0.f};
+        auto load_scales = [&](int kb, float (&dst)[4]) {
+            if constexpr (KIND == KIND_W4A16) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int kcol = kb * kBK + 8 * (4 * half + c);
+                    dst[c] = (n < p.N && kcol < p.K)
+                                 ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + kcol / p.G)))
+                                 : 0.0f;
+                }
+            }
+        };
+        load_scales(0, sc_cur);
+        bool ok = true;
+        for (int kb = 0; kb < p.nk; ++kb) {
+            const int s = kb % kStages;
+            if (kb + 1 < p.nk) load_scales(kb + 1, sc_nxt);
+            if (!wait_or_abort(&sh->tma_full[s], (kb / kStages) & 1, sh, p.status)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *prow = p_tiles + s * kPTile + row * kPRow;
+            uint8_t *arow = a_row + s * kATile;
+            if constexpr (KIND == KIND_W8A8) {
+                const uint4 q0 = *reinterpret_cast<const uint4 *>(prow + 32 * half);
+                const uint4 q1 = *reinterpret_cast<const uint4 *>(prow + 32 * half + 16);
+                const uint32_t wds[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = 4 * half + c;
+                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ rr) << 4)) = conv_w8a8(wds[2 * c], wds[2 * c + 1]);
+                }
+            } else {
+                const uint4 pk = *reinterpret_cast<const uint4 *>(prow + 16 * half);
+                const uint32_t wds[4] = {pk.x, pk.y, pk.z, pk.w};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = 4 * half + c;  // columns kb*64 + 8*chunk .. +7
+                    uint4 v;
+                    if constexpr (KIND == KIND_W4A16) {
+                        v = conv_w4a16(wds[c], sc_cur[c]);
+                    } else {
+                        v = conv_w4a8(wds[c]);
+                    }
+                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ rr) << 4)) = v;
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&sh->conv_full[s]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc_cur[c] = sc_nxt[c];
+        }
+
+        // ---------------- epilogue: TMEM -> registers -> y
+        if (ok) ok = wait_or_abort(&sh->acc_full, 0, sh, p.status);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+        if (ok) {
+            tc_fence_after();
+            const int q = warp & 3;            // TMEM lane quadrant of this warp
+            const int hc = (warp - 2) >> 2;    // column half
+            const int nrow = n0 + 32 * q + lane;
+            float swn = 1.0f;
+            if constexpr (KIND != KIND_W4A16) swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+                const int col0 = 128 * hc + 32 * cc;
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col0, v);
+                if (nrow < p.N) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int m = m0 + col0 + j;
+                        if (m < p.M) {
+                            float out = __uint_as_float(v[j]);
+                            if constexpr (KIND != KIND_W4A16) out = __fmul_rn(__fmul_rn(out, p.sx[m]), swn);
+                            p.y[(size_t)m * p.N + nrow] = out;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// int8 codes [M][K] -> f16 [M][Kx] (Kx = K rounded up to 8, zero padded): exact.
+__global__ void s8_to_f16_kernel(const int8_t *__restrict__ x, uint16_t *__restrict__ out, int64_t M, int64_t K,
+                                 int64_t Kx) {
+    const int64_t groups = M * (Kx / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < groups; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / (Kx / 8), k = (i - m * (Kx / 8)) * 8;
+        uint16_t h[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int v = (k + e < K) ? (int)x[m * K + k + e] : 0;
+            h[e] = __half_as_ushort(__int2half_rn(v));
+        }
+        *reinterpret_cast<uint4 *>(out + m * Kx + k) =
+            make_uint4(h[0] | ((uint32_t)h[1] << 16), h[2] | ((uint32_t)h[3] << 16), h[4] | ((uint32_t)h[5] << 16),
+                       h[6] | ((uint32_t)h[7] << 16));
+    }
+}
+
+constexpr int smem_bytes(int kind) {
+    return 1024 + kStages * (kBM * 128 + kBN * 128 + kBM * (kind == KIND_W8A8 ? 64 : 32)) + 1024;
+}
+
+template <int KIND>
+cudaError_t launch_kernel(const GemmParams &p, cudaStream_t st) {
+    static std::once_flag once;
+    static cudaError_t attr = cudaSuccess;
+    std::call_once(once, [] {
+        attr = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(KIND));
+    });
+    if (attr != cudaSuccess) return attr;
+    dim3 grid((unsigned)ceil_div(p.M, kBN), (unsigned)ceil_div(p.N, kBM));
+    gemm_kernel<KIND><<<grid, kThreads, smem_bytes(KIND), st>>>(p);
+    return cudaGetLastError();
+}
+
+int64_t kx_of(int64_t K) { return round_up(K, 8); }
+
+}  // namespace
+
+bool gemm_supported(const LinearArgs &a) {
+    if (a.M <= 16) return false;
+    if (a.layout != W4_LAYOUT_ROWMAJOR) return false;
+    if (a.N > 0x7FFFFFFF || a.M > 0x7FFFFFFF) return false;
+    if (reinterpret_cast<uintptr_t>(a.w) % 16) return false;
+    const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
+    if (Kb % 16) return false;  // TMA row stride
+    if (a.kind == KIND_W4A16) {
+        if (a.K % 8 || a.G % 8) return false;  // bf16 rows for TMA; one scale per 8 columns
+        if (reinterpret_cast<uintptr_t>(a.x) % 16) return false;
+    } else {
+        // exact integer accumulation in f32 needs 127 * max|q| * K < 2^24
+        if (a.K > (a.kind == KIND_W4A8 ? 16384 : 1024)) return false;
+    }
+    return true;
+}
+
+size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K, int64_t G) {
+    (void)N;
+    (void)G;
+    if (kind == KIND_W4A16 || M <= 16) return 0;
+    return (size_t)(M * kx_of(K) * 2);
+}
+
+cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
+    GemmParams p = {};
+    p.M = (int)a.M;
+    p.N = (int)a.N;
+    p.K = (int)a.K;
+    p.G = (int)a.G;
+    p.ng = (a.kind == KIND_W4A16) ? (int)((a.K + (a.K & 1)) / a.G) : 0;
+    p.y = a.y;
+    p.status = a.status;
+    p.scales = static_cast<const uint16_t *>(a.scale);
+    p.sx = a.sx;
+    p.sw = static_cast<const float *>(a.scale);
+    const void *xsrc = a.x;
+    int64_t Kx = a.K;
+    if (a.kind != KIND_W4A16) {
+        // exact f16 images of the int8 activation codes, in the caller's workspace
+        Kx = kx_of(a.K);
+        const size_t need = (size_t)(a.M * Kx * 2);
+        if (!a.workspace || a.ws_bytes < need) return cudaErrorInvalidValue;
+        const int64_t groups = a.M * (Kx / 8);
+        const int64_t blocks = std::min<int64_t>(ceil_div(groups, 256), 152 * 8);
+        s8_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const int8_t *>(a.x),
+                                                           static_cast<uint16_t *>(a.workspace), a.M, a.K, Kx);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        xsrc = a.workspace;
+    }
+    p.nk = (int)ceil_div(Kx, kBK);
+    {
+        const uint64_t dims[2] = {(uint64_t)Kx, (uint64_t)a.M};
+        const uint64_t strides[1] = {(uint64_t)Kx * 2};
+        const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)kBN};
+        if (!encode_tmap(&p.xmap, a.kind == KIND_W4A16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         2, xsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
+        const uint64_t dims[2] = {(uint64_t)Kb, (uint64_t)a.N};
+        const uint64_t strides[1] = {(uint64_t)Kb};
+        const uint32_t box[2] = {(uint32_t)(a.kind == KIND_W8A8 ? 64 : 32), (uint32_t)kBM};
+        if (!encode_tmap(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    switch (a.kind) {
+        case KIND_W4A16: return launch_kernel<KIND_W4A16>(p, st);
+        case KIND_W4A8: return launch_kernel<KIND_W4A8>(p, st);
+        default: return launch_kernel<KIND_W8A8>(p, st);
+    }
+}
 
 }  // namespace w4
