@@ -165,6 +165,29 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
                                 float *y, int64_t M, int64_t N, int64_t K, int64_t G, int32_t layout,
                                 void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
 
+/* linear_q4 without caller-provided scratch.  No counterpart in the pages
+ * this library follows: it exists for callers that cannot allocate device
+ * memory while they run -- a serving process that reserves its whole memory
+ * budget up front, a host framework whose own allocator owns the device, a
+ * latency-critical loop where an allocation could block.  Same arguments,
+ * result and errors as w4_linear_q4 (flags 0), but the scratch a large batch
+ * needs (M * round_up(K, 8) * 2 bytes when M > 16, see w4_workspace_bytes)
+ * comes from a fixed array inside the library's device image, of
+ * W4_NOALLOC_SCRATCH_BYTES bytes; every GPU that loads the library keeps it
+ * until the process exits.  The function itself calls no allocator.
+ *   - Batches that need more scratch than that return W4_ESHAPE before
+ *     anything is launched.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.  W4_ECUDA if the lookup fails.
+ *   - All calls on a device share the one array and it keeps the last call's
+ *     contents (every call rewrites what it uses before reading it).  Calls
+ *     that can run at the same time on the GPU -- different streams, or
+ *     different host threads -- race on it: order them on one stream. */
+#define W4_NOALLOC_SCRATCH_BYTES (8u << 20)
+w4_status w4_linear_q4_noalloc(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw, float *y,
+                               int64_t M, int64_t N, int64_t K, int32_t layout, void *stream);
+
 /* ---- layout ---------------------------------------------------------------- */
 
 /* pack_interleaved_n64 (vllm-omni "The 4-bit CPU path", "The weight layout,

@@ -34,6 +34,7 @@ SIGNATURES = [
     ("w4_linear_q4", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q8", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
+    ("w4_linear_q4_noalloc", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
     ("w4_workspace_bytes", _sz, [_i32, _i64, _i64, _i64, _i64]),
     ("w4_device_status", _i32, [_vp, _i32]),
@@ -147,6 +148,27 @@ def linear_q4(xq, sx, w, sw, K: int | None = None, N: int | None = None, layout:
     ws, wsb = _workspace(OP_LINEAR_Q4, M, N, K, 0, workspace, xq.device)
     _check(raw.w4_linear_q4(_ptr(xq), _ptr(sx), _ptr(w), _ptr(sw), _ptr(y), M, N, K, layout,
                             _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_q4")
+    return y
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def linear_q4_noalloc(xq, sx, w, sw, K: int | None = None, N: int | None = None, layout: int = LAYOUT_ROWMAJOR,
+                      out=None, stream=None) -> torch.Tensor:
+    """linear_q4 for callers that may not allocate device scratch: large
+    batches use the library's fixed NOALLOC_SCRATCH_BYTES array instead (calls
+    on one device share it, so keep them on one stream).  `out` must be given
+    by callers that may not allocate at all."""
+    M = xq.shape[0]
+    K = xq.shape[1] if K is None else K
+    N = sw.numel() if N is None else N
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    st = raw.w4_linear_q4_noalloc(_ptr(xq), _ptr(sx), _ptr(w), _ptr(sw), _ptr(y), M, N, K, layout, _stream(stream))
+    if st == W4_ESHAPE and raw.w4_workspace_bytes(OP_LINEAR_Q4, M, N, K, 0) > NOALLOC_SCRATCH_BYTES:
+        raise W4Error(st, f"w4_linear_q4_noalloc: batch needs {raw.w4_workspace_bytes(OP_LINEAR_Q4, M, N, K, 0)} "
+                          f"bytes of scratch, above the fixed {NOALLOC_SCRATCH_BYTES}")
+    _check(st, "w4_linear_q4_noalloc")
     return y
 
 
