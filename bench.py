@@ -41,21 +41,39 @@ HBM_FALLBACK_GBS = 6800.0
 
 # ---------------------------------------------------------------- workloads
 
+def _wl(kind, M, N, K, G, layout, desc):
+    return dict(kind=kind, M=M, N=N, K=K, G=G, layout=layout, desc=desc, regime="decode" if M <= 16 else "prefill")
+
+
 WORKLOADS = {
-    "w4a16_gemv_m1": dict(kind="w4a16", M=1, N=2048, K=2048, G=32, layout=0,
-                          desc="group-wise W4A16 GEMV, M=1, K=N=2048, G=32, bf16 x, f16 scales"),
-    "w4a8_gemv_m1": dict(kind="w4a8", M=1, N=2048, K=2048, G=0, layout=0,
-                         desc="W4A8 linear_q4 GEMV, M=1, K=N=2048, per-channel Q4, per-row Q8 x"),
-    "w4a16_decode_m16_n13312": dict(kind="w4a16", M=16, N=13312, K=2048, G=128, layout=0,
-                                    desc="W4A16 decode batch M=16, K=2048, N=13312, G=128"),
-    "w4a16_decode_m1_n13312": dict(kind="w4a16", M=1, N=13312, K=2048, G=128, layout=0,
-                                   desc="W4A16 M=1, K=2048, N=13312 (gate_up shape), G=128"),
-    "w4a8_decode_m1_n13312": dict(kind="w4a8", M=1, N=13312, K=2048, G=0, layout=0,
-                                  desc="W4A8 M=1, K=2048, N=13312 (gate_up shape)"),
-    "w4a16_decode_m1_n13312_il": dict(kind="w4a16", M=1, N=13312, K=2048, G=128, layout=1,
-                                      desc="W4A16 M=1, K=2048, N=13312, G=128, interleaved [N/64][K][32] layout"),
-    "w4a8_decode_m16_n13312": dict(kind="w4a8", M=16, N=13312, K=2048, G=0, layout=0,
-                                   desc="W4A8 decode batch M=16, K=2048, N=13312"),
+    "w4a16_gemv_m1": _wl("w4a16", 1, 2048, 2048, 32, 0,
+                         "group-wise W4A16 GEMV, M=1, K=N=2048, G=32, bf16 x, f16 scales"),
+    "w4a16_gemv_m1_k2047": _wl("w4a16", 1, 2048, 2047, 32, 0,
+                               "group-wise W4A16 GEMV, M=1, K=2047 (odd, padded), N=2048, G=32"),
+    "w4a8_gemv_m1": _wl("w4a8", 1, 2048, 2048, 0, 0,
+                        "W4A8 linear_q4 GEMV, M=1, K=N=2048 (per-row Q8 quantize + linear)"),
+    "w4a16_decode_m16_n13312": _wl("w4a16", 16, 13312, 2048, 128, 0, "W4A16 decode batch M=16, K=2048, N=13312, G=128"),
+    "w4a16_decode_m1_n13312": _wl("w4a16", 1, 13312, 2048, 128, 0, "W4A16 M=1, K=2048, N=13312 (gate_up shape), G=128"),
+    "w4a8_decode_m1_n13312": _wl("w4a8", 1, 13312, 2048, 0, 0, "W4A8 M=1, K=2048, N=13312 (gate_up shape)"),
+    "w4a16_decode_m1_n13312_il": _wl("w4a16", 1, 13312, 2048, 128, 1,
+                                     "W4A16 M=1, K=2048, N=13312, G=128, interleaved [N/64][K][32] layout"),
+    "w4a8_decode_m16_n13312": _wl("w4a8", 16, 13312, 2048, 0, 0, "W4A8 decode batch M=16, K=2048, N=13312"),
+    "w4a8_prefill_m2048_n2048": _wl("w4a8", 2048, 2048, 2048, 0, 0, "W4A8 prefill M=2048, K=2048, N=2048"),
+    "w4a8_prefill_m2048_n3072": _wl("w4a8", 2048, 3072, 2048, 0, 0, "W4A8 prefill M=2048, K=2048, N=3072"),
+    "w4a8_prefill_m2048_n13312": _wl("w4a8", 2048, 13312, 2048, 0, 0, "W4A8 prefill M=2048, K=2048, N=13312"),
+    "w4a16_prefill_m2048_n2048": _wl("w4a16", 2048, 2048, 2048, 128, 0, "W4A16 prefill M=2048, K=2048, N=2048, G=128"),
+    "w4a16_prefill_m2048_n3072": _wl("w4a16", 2048, 3072, 2048, 128, 0, "W4A16 prefill M=2048, K=2048, N=3072, G=128"),
+    "w4a16_prefill_m2048_n13312": _wl("w4a16", 2048, 13312, 2048, 128, 0,
+                                      "W4A16 prefill M=2048, K=2048, N=13312, G=128"),
+}
+
+
+# DRAM bytes (read + write) per launch of the roofline's kernel from one ncu
+# capture (profiles/); None where no capture matches the current kernel.
+TRAFFIC = {
+    "w4a16_gemv_m1": 2395392,                 # profiles/gemv_w4a16_m1_n2048_k2048.md
+    "w4a8_prefill_m2048_n13312": 72658944,    # profiles/gemm_prefill_m2048_n13312_k2048.md
+    "w4a16_prefill_m2048_n13312": 72578816,   # profiles/gemm_prefill_m2048_n13312_k2048.md
 }
 
 
@@ -68,10 +86,28 @@ def weight_bytes(w) -> int:
 
 
 def step_bytes(w) -> int:
-    """Algorithmic bytes of one launch: weights + scales + activations + output."""
+    """Algorithmic bytes of one linear launch: weights + scales + activations + output."""
     M, N, K = w["M"], w["N"], w["K"]
     xb = M * K * (2 if w["kind"] == "w4a16" else 1) + (0 if w["kind"] == "w4a16" else 4 * M)
     return weight_bytes(w) + xb + M * N * 4
+
+
+def step_ops(w) -> int:
+    return 2 * w["M"] * w["N"] * w["K"]
+
+
+def metric_of(w, ms_per_step: float, n_gpus: int = 1):
+    """(value, unit) of the workload's metric for a step time: weight GB/s for
+    decode (M <= 16), tensor ops/s for prefill."""
+    if w["regime"] == "decode":
+        return n_gpus * weight_bytes(w) / (ms_per_step / 1e3) / 1e9, "GB/s"
+    return n_gpus * step_ops(w) / (ms_per_step / 1e3) / 1e12, ("TOPS" if w["kind"] == "w4a8" else "TFLOP/s")
+
+
+def metric_name(w) -> str:
+    if w["regime"] == "decode":
+        return f"int4 linear weight GB/s (M={w['M']} decode)"
+    return f"{'W4A8 TOPS' if w['kind'] == 'w4a8' else 'W4A16 TFLOP/s'} (M={w['M']} prefill)"
 
 
 # ---------------------------------------------------------------- helpers
@@ -179,10 +215,13 @@ def oracle_inputs(w, seed=1001):
 
 
 def time_oracle(w, seconds: float, openmp: bool = True):
-    """Runs the oracle on a bounded sample: whole calls until `seconds` elapse."""
+    """Runs the oracle on a bounded sample: whole calls until `seconds` elapse
+    (prefill: calls on the first 16 activation rows, scaled to ops/s)."""
     import oracle
     o = oracle.get(openmp=openmp)
     cores = os.cpu_count() if openmp else 1
+    if w["regime"] == "prefill":
+        w = dict(w, M=16, regime="prefill")
     if w["kind"] == "w4a16":
         x, wp, s = oracle_inputs(w)
         call = lambda: o.linear_w4a16_lanes(x, wp, s, w["K"], w["G"])
@@ -201,14 +240,22 @@ def time_oracle(w, seconds: float, openmp: bool = True):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    gbs = n * weight_bytes(w) / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n} full calls of {what} on {w['desc']} ({el:.1f} s)"}, n, el
+    value, unit = metric_of(w, el * 1e3 / n)
+    sample = f"{n} full calls of {what} on {w['desc']} ({el:.1f} s)"
+    if w["regime"] == "prefill":
+        sample = f"{n} calls of {what} on 16 of the {w['desc']} activation rows ({el:.1f} s), as ops/s"
+    return {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}, n, el
 
 
 # ---------------------------------------------------------------- GPU measurement
 
 class Workload:
+    """Device-resident inputs for `copies` independent steps of one workload.
+
+    step(i): the whole hot path of the workload on copy i -- W4A16: the
+    linear; W4A8: the per-row Q8 quantizer on f32 activations, then the
+    linear.  kernel(i): the linear alone (the roofline's kernel)."""
+
     def __init__(self, w, copies: int):
         import torch
         from w4a16_int4_quantized_gb300 import ops, synth
@@ -218,26 +265,37 @@ class Workload:
         self.copies = copies
         if w["kind"] == "w4a16":
             x, wp, s = synth.w4a16_inputs(1001, M, N, K, G)
-            self.x = [dev(x) for _ in range(copies)]
-            w0 = dev(wp)
+            x0, w0 = dev(x), dev(wp)
             if w["layout"] == 1:
                 w0 = ops.pack_interleaved_n64(w0, K)
+            self.x = [x0.clone() for _ in range(copies)]
             self.wt = [w0.clone() for _ in range(copies)]
             self.s = [dev(s) for _ in range(copies)]
+            self.ws = None
         else:
             x, W = synth.w4a8_inputs(1001, M, N, K)
-            xq, sx, _ = ops.quantize_row_q8(dev(x))
+            xf = dev(x)
+            xq, sx, _ = ops.quantize_row_q8(xf)
             wq, sw = ops.quantize_matrix_q4(dev(W))
             if w["layout"] == 1:
                 wq = ops.pack_interleaved_n64(wq, K)
+            self.xf = [xf.clone() for _ in range(copies)]
             self.x = [xq.clone() for _ in range(copies)]
             self.sx = [sx.clone() for _ in range(copies)]
             self.wt = [wq.clone() for _ in range(copies)]
             self.s = [sw.clone() for _ in range(copies)]
+            need = ops.workspace_bytes(ops.OP_LINEAR_Q4, M, N, K)
+            self.ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
         self.y = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(copies)]
         torch.cuda.synchronize()
 
-    def launch(self, i: int, flags: int = 1):
+    @property
+    def launches_per_step(self) -> int:
+        if self.w["kind"] == "w4a16":
+            return 1
+        return 2 + (1 if self.ws is not None else 0)  # quantize, (int8 -> f16 prepass), linear
+
+    def kernel(self, i: int, flags: int = 1):
         w, ops = self.w, self.ops
         c = i % self.copies
         if w["kind"] == "w4a16":
@@ -245,31 +303,44 @@ class Workload:
                                    layout=w["layout"], flags=flags, out=self.y[c])
         else:
             ops.linear_q4(self.x[c], self.sx[c], self.wt[c], self.s[c], K=w["K"], N=w["N"],
-                          layout=w["layout"], flags=flags, out=self.y[c])
+                          layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
+
+    def step(self, i: int, flags: int = 1):
+        if self.w["kind"] != "w4a16":
+            c = i % self.copies
+            M, K = self.xf[c].shape
+            st = self.ops.raw.w4_quantize_row_q8(self.xf[c].data_ptr(), M, K, self.x[c].data_ptr(),
+                                                  self.sx[c].data_ptr(), None, self.ops._stream())
+            assert st == 0
+            self.kernel(i, flags=0)  # the quantizer writes x: no early start
+        else:
+            self.kernel(i, flags)
 
 
 def copies_for(w, l2_bytes: int) -> int:
-    per = weight_bytes(w)
-    return max(2, int(np.ceil(2.2 * l2_bytes / per)))
+    per = weight_bytes(w) + w["M"] * w["K"] * (2 if w["kind"] == "w4a16" else 5)
+    return max(2, min(256, int(np.ceil(2.2 * l2_bytes / per))))
 
 
-def time_steps(wl: Workload, steps: int, warmup: int, chunk: int = 256):
-    """Exactly `steps` launches replayed from CUDA graphs; returns (ms, t0, t1)."""
+def time_steps(wl: Workload, steps: int, warmup: int, chunk: int = 256, kernel_only: bool = False):
+    """Exactly `steps` steps replayed from CUDA graphs; returns (ms, t0, t1)."""
     import torch
-    chunk = max(1, min(chunk, steps))
+    chunk = max(1, min(chunk if wl.w["regime"] == "decode" else 8, steps))
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
+
+    run = wl.kernel if kernel_only else wl.step
 
     def capture(n, base):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                wl.launch(base + i)
+                run(base + i)
         return g
 
     with torch.cuda.stream(stream):
         for i in range(min(warmup, 8)):
-            wl.launch(i)
+            run(i)
     torch.cuda.synchronize()
     full = capture(chunk, 0)
     rem = steps % chunk
@@ -335,8 +406,8 @@ def time_e2e(w, steps: int):
     e1.record()
     e1.synchronize()
     ms = e0.elapsed_time(e1)
-    return {"value": steps * weight_bytes(w) / (ms / 1e3) / 1e9, "unit": "GB/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(M * N * 4),
+    value, unit = metric_of(w, ms / steps)
+    return {"value": value, "unit": unit, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(M * N * 4),
             "ms_per_step": ms / steps}
 
 
@@ -346,7 +417,8 @@ def prefill_lines(peaks):
     from w4a16_int4_quantized_gb300 import ops, synth
     out = []
     M, K, G = 2048, 2048, 128
-    bf16_peak = float(peaks.get("bf16_tflops", 1900.0))
+    bf16_peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    int8_peak = ops.probe_mma_peak(0)
     for N in (2048, 3072, 13312):
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
         x, W = synth.w4a8_inputs(1005, M, N, K)
@@ -377,7 +449,10 @@ def prefill_lines(peaks):
                         "value": round(tops, 1), "ms_per_call": round(ms, 4),
                         "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                                      "frac": round(tops / bf16_peak, 4),
-                                     "note": "f16/bf16 tcgen05 path; peak = measured bf16 dense (f16 same rate)"}})
+                                     "note": "f16/bf16 tcgen05 path; peak = measured bf16 dense sustained (f16 same rate)"}})
+            if name == "w4a8":
+                out[-1]["roofline"]["int8_mma_sync_peak_tops"] = round(int8_peak, 1)
+                out[-1]["roofline"]["frac_of_int8_peak"] = round(tops / int8_peak, 3)
         del xq, wq, y, ws, xbd, wbd, sbd
         torch.cuda.empty_cache()
     return out
@@ -417,15 +492,16 @@ def run_reference(args, world, rank):
         cb, n, el = time_oracle(w, per_step)
         total_n += n
         total_s += el
-    value = total_n * weight_bytes(w) / total_s / 1e9
-    cb = dict(cb, value=value, sample=f"{total_n} full oracle calls over {args.steps} steps ({total_s:.1f} s)")
-    line = {"impl": "reference", "metric": "int4 linear weight GB/s (M=1 decode)", "value": value, "unit": "GB/s",
+    ws = dict(w, M=16) if w["regime"] == "prefill" else w   # the sampled rows
+    value, unit = metric_of(ws, total_s * 1e3 / total_n)
+    cb = dict(cb, value=value, sample=f"{total_n} oracle calls over {args.steps} steps ({total_s:.1f} s); " + cb["sample"])
+    line = {"impl": "reference", "metric": metric_name(w), "value": value, "unit": unit,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total_s * 1e3 / max(1, total_n), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload, "desc": w["desc"]},
             "cpu_baseline": cb,
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -471,35 +547,57 @@ def run_ours(args, world, rank, local):
         ms_max = float(t.item())
         dist.barrier()
     status = ops.device_status()
-    value = world * args.steps * weight_bytes(w) / (ms_max / 1e3) / 1e9
-    per_launch_s = ms / 1e3 / args.steps
-    achieved = step_bytes(w) / per_launch_s / 1e9
-    peak = float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))
+    value, unit = metric_of(w, ms_max / args.steps, world)
+    # the roofline's kernel (the linear) timed alone, same graphs and copies
+    kms, _, _ = time_steps(wl, min(args.steps, 4096 if w["regime"] == "decode" else 64), args.warmup,
+                           kernel_only=True)
+    kn = min(args.steps, 4096 if w["regime"] == "decode" else 64)
+    per_launch_s = kms / 1e3 / kn
+    if w["regime"] == "decode":
+        peak = float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))
+        achieved = step_bytes(w) / per_launch_s / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(args.workload), "peak_source": f"{peak_src} hbm_gbs (copy)",
+                "bytes_per_launch": step_bytes(w), "us_per_launch": round(per_launch_s * 1e6, 3)}
+    else:
+        peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+        achieved = step_ops(w) / per_launch_s / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": TRAFFIC.get(args.workload),
+                "peak_source": f"{peak_src} bf16_tflops_sustained (kind::f16 runs at the bf16 rate)",
+                "flops_per_launch": step_ops(w), "us_per_launch": round(per_launch_s * 1e6, 3)}
+        if w["kind"] == "w4a8":
+            # the metric's "% int8 peak": the int8 tensor rate of this part (legacy mma.sync s8), measured now
+            int8 = ops.probe_mma_peak(0)
+            roof["int8_mma_sync_peak_tops"] = round(int8, 1)
+            roof["frac_of_int8_peak"] = round(achieved / int8, 3)
+    launches = args.steps * wl.launches_per_step
     if rank != 0:
         return
     del wl
     torch.cuda.empty_cache()
-    e2e = time_e2e(w, min(args.steps, 2000))
+    e2e = time_e2e(w, min(args.steps, 2000 if w["regime"] == "decode" else 20))
     cpu = None
     if not args.no_cpu:
         cpu, _, _ = time_oracle(w, args.cpu_seconds)
-    extra = [] if args.no_extra else extra_lines(l2, peak) + prefill_lines(peaks)
+    extra = []
+    if not args.no_extra and args.workload == "w4a16_gemv_m1":
+        extra = extra_lines(l2, float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))) + prefill_lines(peaks)
     line = {
-        "metric": "int4 linear weight GB/s (M=1 decode)",
-        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "metric": metric_name(w),
+        "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w["kind"] == "w4a16" else "s8", "data": "synthetic",
         "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"], "N": w["N"], "K": w["K"],
                    "G": w["G"], "parallelism": "replicas" if world > 1 else "single",
-                   "l2": f"inputs larger than L2: {copies} rotating weight copies "
-                         f"({copies * weight_bytes(w) / 2**20:.0f} MiB) vs L2 {l2 / 2**20:.0f} MiB",
-                   "timing": "CUDA events around CUDA-graph replays of exactly `steps` launches"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_source": peak_src,
-                     "bytes_per_launch": step_bytes(w)},
+                   "l2": f"inputs larger than L2: {copies} rotating input copies "
+                         f"({copies * weight_bytes(w) / 2**20:.0f} MiB of weights) vs L2 {l2 / 2**20:.0f} MiB",
+                   "step": "quantize_row_q8 + linear_q4" if w["kind"] == "w4a8" else "linear_w4a16_group",
+                   "timing": "CUDA events around CUDA-graph replays of exactly `steps` steps"},
+        "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": launches,
         "clocks": sampler.summary(t0, t1),
         "device_status": status,
         "extra": extra,

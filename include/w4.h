@@ -214,6 +214,13 @@ int32_t w4_last_cuda_error(void);
 /* Static string for a status code. */
 const char *w4_status_string(w4_status s);
 
+/* Measurement utility (roofline denominators): times a loop of legacy
+ * mma.sync tensor-core instructions on every SM -- kind 0: m16n8k32 s8
+ * (the int8 rate), kind 1: m16n8k16 bf16 -- and returns their throughput in
+ * tera-ops per second.  scratch: device buffer of at least 4 * SMs * 256
+ * int32 (written with junk).  Synchronous.  Not part of any linear. */
+w4_status w4_probe_mma_peak(int32_t kind, int32_t *scratch, int64_t scratch_ints, double *tera_ops, void *stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int32_t w4_version(void);
 

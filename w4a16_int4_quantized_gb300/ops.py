@@ -40,6 +40,7 @@ SIGNATURES = [
     ("w4_device_status", _i32, [_vp, _i32]),
     ("w4_last_cuda_error", _i32, []),
     ("w4_status_string", C.c_char_p, [_i32]),
+    ("w4_probe_mma_peak", _i32, [_i32, _vp, _i64, _vp, _vp]),
     ("w4_version", _i32, []),
 ]
 
@@ -218,6 +219,15 @@ def device_status(clear: bool = False) -> int:
     v = C.c_uint32(0)
     _check(raw.w4_device_status(C.byref(v), 1 if clear else 0), "w4_device_status")
     return int(v.value)
+
+
+def probe_mma_peak(kind: int) -> float:
+    """Measured legacy mma.sync throughput in tera-ops/s (0: s8 m16n8k32, 1: bf16 m16n8k16)."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    scratch = torch.empty(4 * sms * 256, dtype=torch.int32, device="cuda")
+    v = C.c_double(0.0)
+    _check(raw.w4_probe_mma_peak(kind, _ptr(scratch), scratch.numel(), C.byref(v), _stream()), "w4_probe_mma_peak")
+    return float(v.value)
 
 
 def version() -> int:
