@@ -45,6 +45,13 @@ def _wl(kind, M, N, K, G, layout, desc):
     return dict(kind=kind, M=M, N=N, K=K, G=G, layout=layout, desc=desc, regime="decode" if M <= 16 else "prefill")
 
 
+# The microdecoder frame: 5 layers x {q,k,v,o 1024x1024; gate,up 3072x1024;
+# down 1024x3072} x 15 passes of W4A8 linears with per-row Q8 re-quantisation
+# between them (a chain, not one linear: timed by run_microdecoder).
+MICRODECODER = "microdecoder_frame"
+MICRODECODER_DESC = ("W4A8 microdecoder frame: 5 layers x {q,k,v,o 1024x1024; gate,up 3072x1024; down 1024x3072} "
+                     "x 15 passes, per-row Q8 re-quantisation between linears")
+
 WORKLOADS = {
     "w4a16_gemv_m1": _wl("w4a16", 1, 2048, 2048, 32, 0,
                          "group-wise W4A16 GEMV, M=1, K=N=2048, G=32, bf16 x, f16 scales"),
@@ -479,8 +486,34 @@ def extra_lines(l2: int, peak_gbs: float):
 
 # ---------------------------------------------------------------- arms
 
+def run_reference_microdecoder(args):
+    per_step = max(0.5, min(20.0, args.cpu_seconds / max(1, args.steps)))
+    if args.warmup:
+        time_oracle_microdecoder(0.2)
+    total_n, total_s, cb = 0, 0.0, None
+    for _ in range(args.steps):
+        cb, n, el = time_oracle_microdecoder(per_step)
+        total_n += n
+        total_s += el
+    from w4a16_int4_quantized_gb300 import synth
+    ms_frame = total_s * 1e3 / total_n * synth.MICRODECODER_PASSES
+    value = microdecoder_weight_bytes() * synth.MICRODECODER_PASSES / (ms_frame / 1e3) / 1e9
+    cb = dict(cb, value=value, ms_per_frame=ms_frame,
+              sample=f"{total_n} oracle passes over {args.steps} steps ({total_s:.1f} s); " + cb["sample"])
+    line = {"impl": "reference", "metric": "microdecoder effective int4 weight GB/s (frame)", "value": value,
+            "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_frame, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "s8", "data": "synthetic", "config": {"workload": MICRODECODER, "desc": MICRODECODER_DESC},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
+        return
+    if args.workload == MICRODECODER:
+        run_reference_microdecoder(args)
         return
     w = WORKLOADS[args.workload]
     total_n, total_s = 0, 0.0
@@ -502,6 +535,301 @@ def run_reference(args, world, rank):
             "config": {"workload": args.workload, "desc": w["desc"]},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def microdecoder_weight_bytes() -> int:
+    """Packed codes + f32 channel scales of one pass (all 35 linears)."""
+    from w4a16_int4_quantized_gb300 import synth
+    return sum(n * (k // 2) + 4 * n for _, n, k in synth.MICRODECODER_LINEARS) * synth.MICRODECODER_LAYERS
+
+
+def microdecoder_frame_ops(run_linear, run_quant, layers, passes, x0):
+    """The frame's dataflow, shared by the GPU and the oracle legs: per layer
+    q, k, v read h; o reads Q8(v); gate and up read Q8(o); down reads Q8(up);
+    the next h is Q8(down).  run_linear(layer, name, (q, s)) -> y and
+    run_quant(y) -> (q, s) are supplied by the leg."""
+    h = run_quant(x0)
+    y = None
+    for _ in range(passes):
+        for li in range(len(layers)):
+            run_linear(li, "q", h)
+            run_linear(li, "k", h)
+            v = run_quant(run_linear(li, "v", h))
+            o = run_quant(run_linear(li, "o", v))
+            run_linear(li, "gate", o)
+            u = run_quant(run_linear(li, "up", o))
+            y = run_linear(li, "down", u)
+            h = run_quant(y)
+    return h, y
+
+
+class Microdecoder:
+    """Frames of the weight-resident microdecoder through the public API: 35
+    W4A8 linears + 20 per-row re-quantisations per pass, 15 passes, plus the
+    input quantisation; all buffers preallocated so a frame can be captured
+    in a CUDA graph.  `copies` independent weight sets (frame i uses set
+    i % copies) make the working set larger than L2 when asked."""
+
+    def __init__(self, copies: int = 1):
+        import torch
+        from w4a16_int4_quantized_gb300 import ops, synth
+        self.ops, self.synth = ops, synth
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+        self.sets = []
+        for c in range(copies):
+            layers = []
+            for L in synth.microdecoder_weights(3003 + 100 * c):
+                layers.append({name: (*ops.quantize_matrix_q4(dev(W)), W.shape[1]) for name, W in L.items()})
+            self.sets.append(layers)
+        self.x0 = dev(synth.activations_f32(3004, 1, 1024))
+        f = lambda n: torch.empty((1, n), dtype=torch.float32, device="cuda")
+        self.y = {name: f(n) for name, n, _ in synth.MICRODECODER_LINEARS}
+        # the four re-quantisation sites of a layer, in call order: h (x0, then
+        # each down output), v, o, up
+        self.sites = [(torch.empty((1, n), dtype=torch.int8, device="cuda"),
+                       torch.empty(1, dtype=torch.float32, device="cuda")) for n in (1024, 1024, 1024, 3072)]
+        # the chain path writes every linear's own output buffer
+        self.y_chain = [[{name: f(n) for name, n, _ in synth.MICRODECODER_LINEARS}
+                         for _ in range(synth.MICRODECODER_LAYERS)] for _ in range(copies)]
+        self.chain_ws = torch.zeros(ops.workspace_bytes(ops.OP_CHAIN_Q4, 1, 1, 1), dtype=torch.uint8, device="cuda")
+        self.desc = [self.descriptors(c) for c in range(copies)]
+        torch.cuda.synchronize()
+
+    launches_per_frame = {"per_call": 1 + 15 * 5 * 11, "chain": 1}
+
+    def descriptors(self, c: int):
+        """(w, sw, y, input) per linear of weight set c, in the frame's dataflow order."""
+        out = []
+        names = [n for n, _, _ in self.synth.MICRODECODER_LINEARS]
+        for li, L in enumerate(self.sets[c]):
+            base = 7 * li
+            h_in = -1 if li == 0 else base - 1
+            ins = {"q": h_in, "k": h_in, "v": h_in, "o": base + 2, "gate": base + 3, "up": base + 3,
+                   "down": base + 5}
+            out += [(L[n][0], L[n][1], self.y_chain[c][li][n], ins[n]) for n in names]
+        return out
+
+    def frame_chain(self, i: int = 0):
+        """The frame as one w4_chain_q4 call (one persistent kernel)."""
+        c = i % len(self.sets)
+        d = self.desc[c]
+        self.ops.chain_q4(self.x0, d, self.synth.MICRODECODER_PASSES, len(d) - 1, workspace=self.chain_ws)
+        return d[-1][2]
+
+    def frame(self, i: int = 0):
+        ops = self.ops
+        layers = self.sets[i % len(self.sets)]
+        calls = [0]
+
+        def quant(x):
+            q, s = self.sites[calls[0] % 4]
+            calls[0] += 1
+            n = x.shape[1]
+            assert q.shape[1] == n
+            st = ops.raw.w4_quantize_row_q8(x.data_ptr(), 1, n, q.data_ptr(), s.data_ptr(), None, ops._stream())
+            if st != 0:
+                raise RuntimeError(f"w4_quantize_row_q8: status {st}")
+            return q, s
+
+        def linear(li, name, h):
+            pk, sw, K = layers[li][name]
+            return ops.linear_q4(h[0], h[1], pk, sw, K=K, flags=ops.FLAG_PDL, out=self.y[name])
+
+        return microdecoder_frame_ops(linear, quant, layers, self.synth.MICRODECODER_PASSES, self.x0)
+
+
+def time_microdecoder(copies: int, frames: int, warmup: int, mode: str = "chain"):
+    """Exactly `frames` frames replayed from one CUDA graph per weight set;
+    returns (ms_per_frame, t0, t1)."""
+    import torch
+    md = Microdecoder(copies)
+    run = md.frame_chain if mode == "chain" else md.frame
+    st = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        for i in range(min(max(warmup, 1), copies * 2)):
+            run(i)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            run(c)
+        graphs.append(g)
+    with torch.cuda.stream(st):
+        for i in range(max(warmup, 3)):
+            graphs[i % copies].replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for i in range(frames):
+            graphs[i % copies].replay()
+        e1.record(st)
+    e1.synchronize()
+    t1 = time.time()
+    ms = e0.elapsed_time(e1) / frames
+    del graphs, md
+    torch.cuda.empty_cache()
+    return ms, t0, t1
+
+
+def time_microdecoder_e2e(frames: int):
+    """Public API with host buffers: pinned x0 -> device, one frame (one
+    w4_chain_q4 call, replayed from a CUDA graph), the final down output ->
+    pinned host."""
+    import torch
+    md = Microdecoder(1)
+    xh = md.x0.cpu().pin_memory()
+    yh = torch.empty((1, 1024), dtype=torch.float32).pin_memory()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        md.frame_chain(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        y = md.frame_chain(0)
+    torch.cuda.synchronize()
+
+    def step():
+        md.x0.copy_(xh, non_blocking=True)
+        g.replay()
+        yh.copy_(y, non_blocking=True)
+    with torch.cuda.stream(st):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(st):
+        e0.record(st)
+        for _ in range(frames):
+            step()
+        e1.record(st)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / frames
+    del g, md
+    torch.cuda.empty_cache()
+    return ms, xh.numel() * 4, yh.numel() * 4
+
+
+def time_oracle_microdecoder(seconds: float, openmp: bool = True):
+    """The oracle on a bounded sample of the frame: whole passes (35 linears +
+    20 re-quantisations) until `seconds` elapse, scaled to frames."""
+    import oracle
+    from w4a16_int4_quantized_gb300 import synth
+    o = oracle.get(openmp=openmp)
+    layers = [{name: (*o.quantize_matrix_q4(W), W.shape[1]) for name, W in L.items()}
+              for L in synth.microdecoder_weights(3003)]
+    x0 = synth.activations_f32(3004, 1, 1024)
+    linear = lambda li, name, h: o.linear_q4(h[0], h[1], layers[li][name][0], layers[li][name][1], layers[li][name][2])
+    quant = lambda y: o.quantize_row_q8(y)[:2]
+    microdecoder_frame_ops(linear, quant, layers, 1, x0)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        microdecoder_frame_ops(linear, quant, layers, 1, x0)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    ms_frame = el * 1e3 / n * synth.MICRODECODER_PASSES
+    gbs = microdecoder_weight_bytes() * synth.MICRODECODER_PASSES / (ms_frame / 1e3) / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": os.cpu_count() if openmp else 1, "kind": "oracle",
+            "sample": f"{n} whole passes (35 ref_linear_q4 + 20 ref_quantize_row_q8 each) of the frame "
+                      f"({el:.1f} s), scaled x{synth.MICRODECODER_PASSES} to frames",
+            "ms_per_frame": ms_frame}, n, el
+
+
+def microdecoder_line(l2: int, peak_gbs: float, frames: int, warmup: int):
+    """Frame time and effective weight GB/s of the one-kernel chain path and
+    of the per-call path (826 launches), each L2-resident (one weight set,
+    the cache residency that motivates int4 here) and with rotating weight
+    sets larger than L2."""
+    from w4a16_int4_quantized_gb300 import synth
+    wbytes = microdecoder_weight_bytes()
+    per_frame = wbytes * synth.MICRODECODER_PASSES
+    rot = max(2, int(np.ceil(2.2 * l2 / wbytes)))
+    out = {}
+    for mode in ("chain", "per_call"):
+        for label, copies in (("rotating", rot), ("l2_resident", 1)):
+            ms, t0, t1 = time_microdecoder(copies, frames, warmup, mode)
+            out[f"{mode}_{label}"] = {"ms_per_frame": round(ms, 4), "frames_per_s": round(1e3 / ms, 1),
+                                      "weight_gbs": round(per_frame / (ms / 1e3) / 1e9, 1), "weight_sets": copies,
+                                      "frac_of_hbm": round(per_frame / (ms / 1e3) / 1e9 / peak_gbs, 4),
+                                      "launches_per_frame": Microdecoder.launches_per_frame[mode],
+                                      "t0": t0, "t1": t1}
+    return out, wbytes, rot
+
+
+def run_microdecoder(args, world, rank, local):
+    import torch
+    from w4a16_int4_quantized_gb300 import build, synth
+    if local == 0:
+        build.build()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    from w4a16_int4_quantized_gb300 import ops
+    torch.cuda.set_device(local)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 0) or L2_FALLBACK)
+    peaks, peak_src = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))
+    ops.device_status(clear=True)
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    frames = args.steps
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    res, wbytes, rot = microdecoder_line(l2, peak, frames, args.warmup)
+    time.sleep(0.2)
+    sampler.stop()
+    r = res["chain_rotating"]
+    ms = r["ms_per_frame"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = ops.device_status()
+    if rank != 0:
+        return
+    per_frame = wbytes * synth.MICRODECODER_PASSES
+    value = world * per_frame / (ms / 1e3) / 1e9
+    e_ms, h2d, d2h = time_microdecoder_e2e(min(frames, 200))
+    cpu = None
+    if not args.no_cpu:
+        cpu, _, _ = time_oracle_microdecoder(args.cpu_seconds)
+    line = {"metric": "microdecoder effective int4 weight GB/s (frame)", "value": round(value, 1), "unit": "GB/s",
+            "n_gpus": world, "steps": frames, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+            "config": {"workload": MICRODECODER, "desc": MICRODECODER_DESC,
+                       "step": "one frame = one w4_chain_q4 call (one persistent kernel)",
+                       "weight_bytes_per_pass": wbytes, "passes_per_frame": synth.MICRODECODER_PASSES,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": f"inputs larger than L2: {rot} rotating weight sets ({rot * wbytes / 2**20:.0f} MiB) "
+                             f"vs L2 {l2 / 2**20:.0f} MiB",
+                       "timing": "CUDA events around CUDA-graph replays of exactly `steps` frames"},
+            "paths": {k: {kk: vv for kk, vv in v.items() if kk not in ("t0", "t1")} for k, v in res.items()},
+            "roofline": {"bound": "hbm", "achieved": round(per_frame / (ms / 1e3) / 1e9, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(per_frame / (ms / 1e3) / 1e9 / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_src} hbm_gbs (copy)",
+                         "note": "weight bytes of the whole frame / frame time of the one-kernel chain; "
+                                 "bound by the 299 grid barriers between dependent stages, not by bytes"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(per_frame / (e_ms / 1e3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
+            "gpu_launches": frames * Microdecoder.launches_per_frame["chain"],
+            "clocks": sampler.summary(r["t0"], r["t1"]),
+            "device_status": status}
     print(json.dumps(line), flush=True)
 
 
@@ -583,6 +911,9 @@ def run_ours(args, world, rank, local):
     extra = []
     if not args.no_extra and args.workload == "w4a16_gemv_m1":
         extra = extra_lines(l2, float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))) + prefill_lines(peaks)
+        md, _, _ = microdecoder_line(l2, float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS)), 200, 3)
+        extra.append({"workload": MICRODECODER, "desc": MICRODECODER_DESC, "metric": "effective int4 weight GB/s",
+                      **{k: {kk: vv for kk, vv in v.items() if kk not in ("t0", "t1")} for k, v in md.items()}})
     line = {
         "metric": metric_name(w),
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -611,7 +942,7 @@ def main():
     ap.add_argument("--steps", type=int, default=65536)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="w4a16_gemv_m1")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + [MICRODECODER], default="w4a16_gemv_m1")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
@@ -622,7 +953,10 @@ def main():
         run_reference(args, world, rank)
         return
     world, rank, local = dist_setup(args.gpus)
-    run_ours(args, world, rank, local)
+    if args.workload == MICRODECODER:
+        run_microdecoder(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

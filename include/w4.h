@@ -75,7 +75,7 @@ enum {
 };
 
 /* Operation ids for w4_workspace_bytes. */
-enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2 };
+enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2, W4_OP_CHAIN_Q4 = 3 };
 
 /* ---- quantizers ------------------------------------------------------------ */
 
@@ -188,6 +188,56 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
 w4_status w4_linear_q4_noalloc(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw, float *y,
                                int64_t M, int64_t N, int64_t K, int32_t layout, void *stream);
 
+/* ---- weight-resident chains -------------------------------------------------- */
+
+/* The microdecoder of docs.rs ftts_kernels::int4 ("Why the microdecoder"): a
+ * small decoder body whose int4 weights are re-read many times per frame,
+ * each linear fed by the per-row Q8 quantisation of an earlier linear's
+ * output.  w4_chain_q4 runs such a chain -- every linear, every pass -- as
+ * ONE persistent kernel (one CTA per SM, a grid barrier between dependent
+ * steps), in place of one quantize_row_q8 + linear_q4 launch per step. */
+#define W4_CHAIN_MAX_LINEARS 64
+#define W4_CHAIN_MAX_K 8192
+
+/* One W4A8 linear of a chain at M = 1. */
+typedef struct w4_chain_linear {
+    const uint8_t *w; /* packed biased Q4 [N][K/2], row-major (quantize_matrix_q4), 16-byte aligned */
+    const float *sw;  /* [N] per-channel scales */
+    float *y;         /* [N] f32 output, 16-byte aligned; after the call it holds the last pass's value */
+    int32_t N;        /* output channels, >= 1 */
+    int32_t K;        /* input length: K0 when input == -1, else N of the input linear; K % 32 == 0 */
+    int32_t input;    /* -1: the pass input; else the index (< this one's) of the linear whose y is read */
+    int32_t reserved; /* must be 0 */
+} w4_chain_linear;
+
+/* chain_q4: h = x0 (length K0); for each of `passes` passes, for i = 0 ..
+ * n_lin - 1 in order:
+ *     in_i = (lin[i].input < 0) ? h : lin[lin[i].input].y
+ *     (q, sx) = quantize_row_q8(in_i)           -- as w4_quantize_row_q8
+ *     lin[i].y = linear_q4(q, sx, lin[i].w, lin[i].sw)   -- as w4_linear_q4, M = 1
+ * and at the end of the pass h = lin[pass_output].y.  Every output is bit-
+ * identical to that sequence of w4_quantize_row_q8 / w4_linear_q4 calls.
+ *   lin: HOST array of n_lin descriptors (1 <= n_lin <= W4_CHAIN_MAX_LINEARS),
+ *     read during the call only.  x0, w, sw, y: device pointers; the y
+ *     buffers must not overlap each other, x0, or any weights.
+ *   Linears are grouped by depth (depth 0 reads the pass input; a linear
+ *   reading linear j has depth(j) + 1); all linears of one depth must read the
+ *   same vector (W4_ESHAPE otherwise).
+ *   workspace: at least w4_workspace_bytes(W4_OP_CHAIN_Q4, ...) bytes of
+ *   device scratch (the barrier counter), not used by concurrent work.
+ * Errors (before any launch): n_lin out of range, passes < 0, K0 <= 0, a
+ * descriptor with N <= 0, K <= 0, input outside [-1, i) or reserved != 0,
+ * pass_output outside [0, n_lin) -> W4_EINVAL; K0 or a K not a multiple of
+ * 32 or above W4_CHAIN_MAX_K, a K that is not its input's length, passes > 1
+ * with lin[pass_output].N != K0 or pass_output of depth 0, or the depth rule
+ * broken -> W4_ESHAPE; passes == 0 -> W4_OK, nothing launched; a NULL
+ * pointer, x0 / w / y not 16-byte aligned, or workspace too small ->
+ * W4_EINVAL; the device cannot keep one CTA per SM resident -> W4_ECUDA.
+ * A barrier wait that runs out (about one second) sets status bit 4 and the
+ * kernel returns. */
+w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
+                      int32_t pass_output, void *workspace, size_t ws_bytes, void *stream);
+
 /* ---- layout ---------------------------------------------------------------- */
 
 /* pack_interleaved_n64 (vllm-omni "The 4-bit CPU path", "The weight layout,
@@ -205,7 +255,7 @@ size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G
 /* Reads (and when clear != 0, clears) the device status word of the
  * current device: 0 when no kernel has given up on a bounded wait.  Bits:
  * 1 = a weight-tile copy wait timed out, 2 = a tensor-core pipeline wait
- * timed out.  Synchronous (a small device-to-host copy). */
+ * timed out, 4 = a chain_q4 grid-barrier wait timed out.  Synchronous (a small device-to-host copy). */
 w4_status w4_device_status(uint32_t *out, int32_t clear);
 
 /* The cudaError_t (as int) behind the last W4_ECUDA of this thread. */

@@ -106,3 +106,35 @@ def test_workspace_query_is_host_only(lib):
     for op in (lib.OP_LINEAR_Q4, lib.OP_LINEAR_Q8, lib.OP_LINEAR_W4A16):
         assert lib.workspace_bytes(op, 1, 2048, 2048, 128) == 0        # decode needs no scratch
         assert lib.workspace_bytes(op, 2048, 2048, 2048, 128) >= 0
+
+
+def test_chain_validation(lib):
+    """w4_chain_q4 rejects malformed chains on the host, in the header's order."""
+    r = lib.raw
+    mk = lambda *rows: (lib.ChainLinear * len(rows))(*[lib.ChainLinear(0x1000, 0x2000, 0x3000, N, K, inp, 0)
+                                                         for N, K, inp in rows])
+    ws = C.c_void_p(0x4000)
+    f = lambda arr, n=None, K0=64, passes=2, po=None, x0=FAKE, wsb=256: r.w4_chain_q4(
+        x0, K0, arr, len(arr) if n is None else n, passes, (len(arr) - 1) if po is None else po, ws, wsb, None)
+    ok = mk((96, 64, -1), (64, 96, 0))                    # h(64) -> 96 -> 64 = next h
+    assert f(ok, passes=0) == lib.W4_OK                   # nothing to run: no launch
+    assert f(ok, n=0) == lib.W4_EINVAL
+    assert f(ok, n=65) == lib.W4_EINVAL
+    assert f(ok, passes=-1) == lib.W4_EINVAL
+    assert f(ok, K0=0) == lib.W4_EINVAL
+    assert f(ok, po=2) == lib.W4_EINVAL
+    assert f(mk((96, 64, 0), (64, 96, 0))) == lib.W4_EINVAL            # input must be an earlier linear
+    assert f(mk((96, 64, -1), (64, 96, -2))) == lib.W4_EINVAL
+    bad = mk((96, 64, -1), (64, 96, 0))
+    bad[1].reserved = 1
+    assert f(bad) == lib.W4_EINVAL
+    assert f(mk((96, 48, -1), (48, 96, 0)), K0=48) == lib.W4_ESHAPE    # K % 32
+    assert f(mk((96, 64, -1), (64, 64, 0))) == lib.W4_ESHAPE            # K is not the input's length
+    assert f(mk((96, 64, -1), (32, 96, 0))) == lib.W4_ESHAPE            # pass output N != K0 with passes > 1
+    assert f(mk((64, 64, -1), (64, 64, 0)), po=0) == lib.W4_ESHAPE     # pass output of depth 0 races its readers
+    # depth rule: the two depth-1 linears read different vectors
+    assert f(mk((64, 64, -1), (64, 64, -1), (64, 64, 0), (64, 64, 1)), po=3) == lib.W4_ESHAPE
+    assert f(ok, x0=None) == lib.W4_EINVAL
+    assert f(ok, x0=C.c_void_p(0x1004)) == lib.W4_EINVAL                # x0 not 16-byte aligned
+    assert f(ok, wsb=8) == lib.W4_EINVAL                                 # workspace too small
+    assert lib.workspace_bytes(lib.OP_CHAIN_Q4, 1, 1, 1) > 0

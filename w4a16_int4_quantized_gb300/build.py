@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw4gb300.so")
-SOURCES = ["capi.cu", "quant.cu", "gemv.cu", "gemm_tc.cu", "tmap.cu", "noalloc.cu", "peaks.cu"]
+SOURCES = ["capi.cu", "quant.cu", "gemv.cu", "gemm_tc.cu", "tmap.cu", "noalloc.cu", "peaks.cu", "chain.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

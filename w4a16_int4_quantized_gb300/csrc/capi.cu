@@ -199,7 +199,42 @@ w4_status w4_pack_interleaved_n64(const uint8_t *w_rowmajor, uint8_t *w_il, int6
     return cuda_status(w4::launch_pack_n64(w_rowmajor, w_il, N, K, as_stream(stream)));
 }
 
+w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
+                      int32_t pass_output, void *workspace, size_t ws_bytes, void *stream) {
+    if (n_lin < 1 || n_lin > W4_CHAIN_MAX_LINEARS || passes < 0 || K0 <= 0 || !lin) return W4_EINVAL;
+    if (pass_output < 0 || pass_output >= n_lin) return W4_EINVAL;
+    for (int32_t i = 0; i < n_lin; ++i) {
+        const w4_chain_linear &L = lin[i];
+        if (L.N <= 0 || L.K <= 0 || L.input < -1 || L.input >= i || L.reserved != 0) return W4_EINVAL;
+    }
+    if (K0 % 32 || K0 > W4_CHAIN_MAX_K) return W4_ESHAPE;
+    for (int32_t i = 0; i < n_lin; ++i) {
+        const w4_chain_linear &L = lin[i];
+        if (L.K % 32 || L.K > W4_CHAIN_MAX_K) return W4_ESHAPE;
+        if (L.K != (L.input < 0 ? K0 : lin[L.input].N)) return W4_ESHAPE;
+    }
+    if (passes > 1 && lin[pass_output].N != K0) return W4_ESHAPE;
+    if (!w4::chain_stages_ok(lin, n_lin, passes, pass_output)) return W4_ESHAPE;
+    if (passes == 0) return W4_OK;
+    auto misaligned = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15) != 0; };
+    if (!x0 || misaligned(x0)) return W4_EINVAL;
+    for (int32_t i = 0; i < n_lin; ++i) {
+        const w4_chain_linear &L = lin[i];
+        if (!L.w || !L.sw || !L.y || misaligned(L.w) || misaligned(L.y)) return W4_EINVAL;
+    }
+    const w4_status ws = check_workspace(W4_OP_CHAIN_Q4, 1, 1, K0, 0, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    uint32_t *status = nullptr;
+    cudaError_t e = status_ptr(&status);
+    if (e != cudaSuccess) return cuda_status(e);
+    const int rc = w4::chain_plan_launch(x0, K0, lin, n_lin, passes, pass_output, workspace, status,
+                                         as_stream(stream), &e);
+    if (rc == W4_ECUDA) return cuda_status(e);
+    return (w4_status)rc;
+}
+
 size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G) {
+    if (op == W4_OP_CHAIN_Q4) return w4::kChainWorkspaceBytes;
     if (M <= 16 || N <= 0 || K <= 0) return 0;
     switch (op) {
         case W4_OP_LINEAR_Q4: return w4::gemm_workspace_bytes(w4::KIND_W4A8, M, N, K, G);

@@ -19,6 +19,7 @@ namespace w4 {
 // Status-word bits (mirrored in include/w4.h, w4_device_status).
 constexpr uint32_t kStatusCopyTimeout = 1u;
 constexpr uint32_t kStatusPipeTimeout = 2u;
+constexpr uint32_t kStatusBarrierTimeout = 4u;
 
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;

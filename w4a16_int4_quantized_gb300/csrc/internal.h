@@ -6,6 +6,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "w4.h"
+
 namespace w4 {
 
 enum Kind : int { KIND_W4A8 = 0, KIND_W8A8 = 1, KIND_W4A16 = 2 };
@@ -48,5 +50,18 @@ cudaError_t launch_generic(const LinearArgs &a, cudaStream_t st);
 bool gemm_supported(const LinearArgs &a);
 size_t gemm_workspace_bytes(int kind, int64_t M, int64_t N, int64_t K, int64_t G);
 cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st);
+
+// chain.cu -- a chain of M = 1 W4A8 linears as one persistent cooperative kernel.
+constexpr int kChainMaxLinears = W4_CHAIN_MAX_LINEARS;
+constexpr int kChainMaxK = W4_CHAIN_MAX_K;
+constexpr int64_t kChainMaxStageRows = (int64_t)1 << 24;
+constexpr size_t kChainWorkspaceBytes = 256;
+// Host check: linears of one depth read one vector, stage rows bounded, and
+// with passes > 1 the pass output is not of depth 0.
+bool chain_stages_ok(const w4_chain_linear *lin, int32_t n_lin, int32_t passes, int32_t pass_output);
+// Plans (stages by depth) and launches a validated chain; returns a w4_status
+// (W4_ESHAPE when the chain has no stage structure), *err the CUDA error.
+int chain_plan_launch(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
+                      int32_t pass_output, void *workspace, uint32_t *status, cudaStream_t st, cudaError_t *err);
 
 }  // namespace w4

@@ -22,7 +22,15 @@ LIB_PATH = os.path.join(_HERE, "libw4gb300.so")
 W4_OK, W4_EINVAL, W4_ESHAPE, W4_ECUDA = 0, 1, 2, 3
 LAYOUT_ROWMAJOR, LAYOUT_N64 = 0, 1
 FLAG_PDL = 1
-OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16 = 0, 1, 2
+OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16, OP_CHAIN_Q4 = 0, 1, 2, 3
+CHAIN_MAX_LINEARS, CHAIN_MAX_K = 64, 8192
+
+
+class ChainLinear(C.Structure):
+    """w4_chain_linear of include/w4.h."""
+    _fields_ = [("w", C.c_void_p), ("sw", C.c_void_p), ("y", C.c_void_p),
+                ("N", C.c_int32), ("K", C.c_int32), ("input", C.c_int32), ("reserved", C.c_int32)]
+
 
 # (name, restype, argtypes) of every exported symbol, in header order.
 _vp, _i64, _i32, _u32, _sz = C.c_void_p, C.c_int64, C.c_int32, C.c_uint32, C.c_size_t
@@ -35,6 +43,7 @@ SIGNATURES = [
     ("w4_linear_q8", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_noalloc", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    ("w4_chain_q4", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
     ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
     ("w4_workspace_bytes", _sz, [_i32, _i64, _i64, _i64, _i64]),
     ("w4_device_status", _i32, [_vp, _i32]),
@@ -201,6 +210,24 @@ def linear_w4a16_group(x, w, scales, G: int, K: int | None = None, N: int | None
     _check(raw.w4_linear_w4a16_group(_ptr(x), _ptr(w), _ptr(scales), _ptr(y), M, N, K, G, layout,
                                      _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_w4a16_group")
     return y
+
+
+def chain_q4(x0, linears, passes: int, pass_output: int, workspace=None, stream=None):
+    """Runs a chain of M = 1 W4A8 linears as one kernel.  linears: sequence of
+    (w, sw, y, input) with w packed [N][K/2] uint8, sw [N] f32, y [N] f32
+    (written), input = -1 for the pass input or the index of an earlier
+    linear.  Returns the y tensors."""
+    arr = (ChainLinear * len(linears))()
+    for i, (w, sw, y, inp) in enumerate(linears):
+        N = sw.numel()
+        K = 2 * w.shape[-1] if w.dim() == 2 else 0
+        arr[i] = ChainLinear(_ptr(w), _ptr(sw), _ptr(y), N, K, inp, 0)
+    if workspace is None:
+        workspace = torch.empty(raw.w4_workspace_bytes(OP_CHAIN_Q4, 1, 1, 1, 0), dtype=torch.uint8,
+                                device=x0.device)
+    _check(raw.w4_chain_q4(_ptr(x0), x0.numel(), arr, len(linears), passes, pass_output, _ptr(workspace),
+                           workspace.numel(), _stream(stream)), "w4_chain_q4")
+    return [y for _, _, y, _ in linears]
 
 
 def pack_interleaved_n64(w: torch.Tensor, K: int, stream=None) -> torch.Tensor:
