@@ -592,8 +592,8 @@ class Microdecoder:
         # the chain path writes every linear's own output buffer
         self.y_chain = [[{name: f(n) for name, n, _ in synth.MICRODECODER_LINEARS}
                          for _ in range(synth.MICRODECODER_LAYERS)] for _ in range(copies)]
-        self.chain_ws = torch.zeros(ops.workspace_bytes(ops.OP_CHAIN_Q4, 1, 1, 1), dtype=torch.uint8, device="cuda")
         self.desc = [self.descriptors(c) for c in range(copies)]
+        self.chain_ws = torch.zeros(ops.chain_workspace_bytes(self.desc[0], 1024), dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
 
     launches_per_frame = {"per_call": 1 + 15 * 5 * 11, "chain": 1}

@@ -75,7 +75,7 @@ enum {
 };
 
 /* Operation ids for w4_workspace_bytes. */
-enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2, W4_OP_CHAIN_Q4 = 3 };
+enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2 };
 
 /* ---- quantizers ------------------------------------------------------------ */
 
@@ -194,8 +194,9 @@ w4_status w4_linear_q4_noalloc(const int8_t *xq, const float *sx, const uint8_t 
  * small decoder body whose int4 weights are re-read many times per frame,
  * each linear fed by the per-row Q8 quantisation of an earlier linear's
  * output.  w4_chain_q4 runs such a chain -- every linear, every pass -- as
- * ONE persistent kernel (one CTA per SM, a grid barrier between dependent
- * steps), in place of one quantize_row_q8 + linear_q4 launch per step. */
+ * ONE persistent kernel (one CTA per SM; inside a pass each step waits only
+ * for the tagged elements it reads, a grid barrier separates passes), in
+ * place of one quantize_row_q8 + linear_q4 launch per step. */
 #define W4_CHAIN_MAX_LINEARS 64
 #define W4_CHAIN_MAX_K 8192
 
@@ -223,20 +224,27 @@ typedef struct w4_chain_linear {
  *   Linears are grouped by depth (depth 0 reads the pass input; a linear
  *   reading linear j has depth(j) + 1); all linears of one depth must read the
  *   same vector (W4_ESHAPE otherwise).
- *   workspace: at least w4_workspace_bytes(W4_OP_CHAIN_Q4, ...) bytes of
- *   device scratch (the barrier counter), not used by concurrent work.
+ *   workspace: at least w4_chain_workspace_bytes(lin, n_lin, K0) bytes of
+ *   device scratch (a barrier counter and tagged copies of the vectors the
+ *   chain passes along), 16-byte aligned, not used by concurrent work; the
+ *   call clears it on `stream` before the kernel.
  * Errors (before any launch): n_lin out of range, passes < 0, K0 <= 0, a
  * descriptor with N <= 0, K <= 0, input outside [-1, i) or reserved != 0,
  * pass_output outside [0, n_lin) -> W4_EINVAL; K0 or a K not a multiple of
  * 32 or above W4_CHAIN_MAX_K, a K that is not its input's length, passes > 1
  * with lin[pass_output].N != K0 or pass_output of depth 0, or the depth rule
  * broken -> W4_ESHAPE; passes == 0 -> W4_OK, nothing launched; a NULL
- * pointer, x0 / w / y not 16-byte aligned, or workspace too small ->
- * W4_EINVAL; the device cannot keep one CTA per SM resident -> W4_ECUDA.
- * A barrier wait that runs out (about one second) sets status bit 4 and the
- * kernel returns. */
+ * pointer, x0 / w / y / workspace not 16-byte aligned, or workspace too
+ * small -> W4_EINVAL; the device cannot keep one CTA per SM resident ->
+ * W4_ECUDA.  A wait (for an input element or at a pass barrier) that runs
+ * out, about one second, sets status bit 4 and the kernel returns. */
 w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
                       int32_t pass_output, void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of workspace w4_chain_q4 needs for this chain: 256 + 8 * (2 * K0 +
+ * the N of every linear some other linear reads).  Host only; 0 when lin is
+ * NULL or n_lin is out of range. */
+size_t w4_chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32_t K0);
 
 /* ---- layout ---------------------------------------------------------------- */
 
@@ -255,7 +263,7 @@ size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G
 /* Reads (and when clear != 0, clears) the device status word of the
  * current device: 0 when no kernel has given up on a bounded wait.  Bits:
  * 1 = a weight-tile copy wait timed out, 2 = a tensor-core pipeline wait
- * timed out, 4 = a chain_q4 grid-barrier wait timed out.  Synchronous (a small device-to-host copy). */
+ * timed out, 4 = a chain_q4 wait (input element or pass barrier) timed out.  Synchronous (a small device-to-host copy). */
 w4_status w4_device_status(uint32_t *out, int32_t clear);
 
 /* The cudaError_t (as int) behind the last W4_ECUDA of this thread. */

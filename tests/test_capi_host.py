@@ -114,7 +114,7 @@ def test_chain_validation(lib):
     mk = lambda *rows: (lib.ChainLinear * len(rows))(*[lib.ChainLinear(0x1000, 0x2000, 0x3000, N, K, inp, 0)
                                                          for N, K, inp in rows])
     ws = C.c_void_p(0x4000)
-    f = lambda arr, n=None, K0=64, passes=2, po=None, x0=FAKE, wsb=256: r.w4_chain_q4(
+    f = lambda arr, n=None, K0=64, passes=2, po=None, x0=FAKE, wsb=1 << 20: r.w4_chain_q4(
         x0, K0, arr, len(arr) if n is None else n, passes, (len(arr) - 1) if po is None else po, ws, wsb, None)
     ok = mk((96, 64, -1), (64, 96, 0))                    # h(64) -> 96 -> 64 = next h
     assert f(ok, passes=0) == lib.W4_OK                   # nothing to run: no launch
@@ -136,5 +136,7 @@ def test_chain_validation(lib):
     assert f(mk((64, 64, -1), (64, 64, -1), (64, 64, 0), (64, 64, 1)), po=3) == lib.W4_ESHAPE
     assert f(ok, x0=None) == lib.W4_EINVAL
     assert f(ok, x0=C.c_void_p(0x1004)) == lib.W4_EINVAL                # x0 not 16-byte aligned
-    assert f(ok, wsb=8) == lib.W4_EINVAL                                 # workspace too small
-    assert lib.workspace_bytes(lib.OP_CHAIN_Q4, 1, 1, 1) > 0
+    need = r.w4_chain_workspace_bytes(ok, 2, 64)
+    assert need == 256 + 8 * (2 * 64 + 96)                              # header + pass output x2 + linear 0
+    assert f(ok, wsb=need - 1) == lib.W4_EINVAL                          # workspace too small
+    assert r.w4_chain_workspace_bytes(None, 2, 64) == 0

@@ -221,3 +221,41 @@ def test_chain_zero_input_and_noop(ops, ora):
     for _, _, y, _ in glins:
         assert torch.equal(y.view(torch.int32), torch.zeros_like(y).view(torch.int32))
     assert ops.device_status() == 0
+
+
+def _tie_inputs(amax: float, K: int, seed: int) -> np.ndarray:
+    """x0 with max |x0| = amax, the rest exact and near half-integer multiples
+    of the Q8 scale fl(amax / 127): the values whose code depends on the last
+    bit of the quotient and on ties-to-even."""
+    sx = np.float32(np.float32(amax) / np.float32(127))
+    vals = [np.float32(amax)]
+    for k in range(-127, 127):
+        h = np.float32((k + 0.5) * float(sx))
+        vals += [h, np.nextafter(h, np.float32(np.inf)), np.nextafter(h, np.float32(-np.inf))]
+    vals = np.array(vals, np.float32)
+    rng = np.random.default_rng(seed)
+    vals = np.concatenate([vals, rng.uniform(-amax, amax, K).astype(np.float32)])[:K]
+    vals[0] = np.float32(amax)
+    return vals
+
+
+@pytest.mark.parametrize("amax", [127.0, 100.0, 3.0e-3])
+def test_chain_quantizer_ties(ops, ora, amax):
+    """Unit-vector weights make y reveal every Q8 code of the chain's input
+    (y_n = 7 q_n sx / 7 exactly per channel); a second linear re-quantises
+    that output.  Bit-exact against the oracle's quantize_row_q8 + linear_q4."""
+    K = 1024
+    W = np.zeros((K, K), np.float32)
+    W[np.arange(K), np.arange(K)] = 1.0
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    pk, sw = ops.quantize_matrix_q4(dev(W))
+    W2 = synth.weights_f32(4300, 64, K)
+    pk2, sw2 = ops.quantize_matrix_q4(dev(W2))
+    x0 = _tie_inputs(amax, K, 4301)
+    ys = [torch.empty((1, K), device="cuda"), torch.empty((1, 64), device="cuda")]
+    ops.chain_q4(dev(x0), [(pk, sw, ys[0], -1), (pk2, sw2, ys[1], 0)], 1, 1)
+    ref = oracle_chain(ora, x0, [ora.quantize_matrix_q4(W) + (-1,), ora.quantize_matrix_q4(W2) + (0,)], 1, 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(ys[0].cpu().numpy().view(np.uint32), ref[0].view(np.uint32))
+    assert np.array_equal(ys[1].cpu().numpy().view(np.uint32), ref[1].view(np.uint32))
+    assert ops.device_status() == 0

@@ -222,8 +222,8 @@ w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, i
         const w4_chain_linear &L = lin[i];
         if (!L.w || !L.sw || !L.y || misaligned(L.w) || misaligned(L.y)) return W4_EINVAL;
     }
-    const w4_status ws = check_workspace(W4_OP_CHAIN_Q4, 1, 1, K0, 0, workspace, ws_bytes);
-    if (ws != W4_OK) return ws;
+    if (!workspace || misaligned(workspace) || ws_bytes < w4::chain_workspace_bytes(lin, n_lin, K0))
+        return W4_EINVAL;
     uint32_t *status = nullptr;
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_status(e);
@@ -233,8 +233,12 @@ w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, i
     return (w4_status)rc;
 }
 
+size_t w4_chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32_t K0) {
+    if (!lin || n_lin < 1 || n_lin > W4_CHAIN_MAX_LINEARS || K0 < 0) return 0;
+    return w4::chain_workspace_bytes(lin, n_lin, K0);
+}
+
 size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G) {
-    if (op == W4_OP_CHAIN_Q4) return w4::kChainWorkspaceBytes;
     if (M <= 16 || N <= 0 || K <= 0) return 0;
     switch (op) {
         case W4_OP_LINEAR_Q4: return w4::gemm_workspace_bytes(w4::KIND_W4A8, M, N, K, G);

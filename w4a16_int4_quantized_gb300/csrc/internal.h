@@ -55,7 +55,9 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st);
 constexpr int kChainMaxLinears = W4_CHAIN_MAX_LINEARS;
 constexpr int kChainMaxK = W4_CHAIN_MAX_K;
 constexpr int64_t kChainMaxStageRows = (int64_t)1 << 24;
-constexpr size_t kChainWorkspaceBytes = 256;
+constexpr size_t kChainHeaderBytes = 256;
+// Workspace of a chain: header + tagged pass output [2][K0] + tagged copies of read linears.
+size_t chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32_t K0);
 // Host check: linears of one depth read one vector, stage rows bounded, and
 // with passes > 1 the pass output is not of depth 0.
 bool chain_stages_ok(const w4_chain_linear *lin, int32_t n_lin, int32_t passes, int32_t pass_output);

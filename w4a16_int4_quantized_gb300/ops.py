@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libw4gb300.so")
 W4_OK, W4_EINVAL, W4_ESHAPE, W4_ECUDA = 0, 1, 2, 3
 LAYOUT_ROWMAJOR, LAYOUT_N64 = 0, 1
 FLAG_PDL = 1
-OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16, OP_CHAIN_Q4 = 0, 1, 2, 3
+OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16 = 0, 1, 2
 CHAIN_MAX_LINEARS, CHAIN_MAX_K = 64, 8192
 
 
@@ -44,6 +44,7 @@ SIGNATURES = [
     ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_noalloc", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     ("w4_chain_q4", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
+    ("w4_chain_workspace_bytes", _sz, [_vp, _i32, _i32]),
     ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
     ("w4_workspace_bytes", _sz, [_i32, _i64, _i64, _i64, _i64]),
     ("w4_device_status", _i32, [_vp, _i32]),
@@ -212,19 +213,27 @@ def linear_w4a16_group(x, w, scales, G: int, K: int | None = None, N: int | None
     return y
 
 
+def chain_descriptors(linears):
+    """ctypes array of w4_chain_linear for (w, sw, y, input) tuples."""
+    arr = (ChainLinear * len(linears))()
+    for i, (w, sw, y, inp) in enumerate(linears):
+        arr[i] = ChainLinear(_ptr(w), _ptr(sw), _ptr(y), sw.numel(), 2 * w.shape[-1], inp, 0)
+    return arr
+
+
+def chain_workspace_bytes(linears, K0: int) -> int:
+    return raw.w4_chain_workspace_bytes(chain_descriptors(linears), len(linears), K0)
+
+
 def chain_q4(x0, linears, passes: int, pass_output: int, workspace=None, stream=None):
     """Runs a chain of M = 1 W4A8 linears as one kernel.  linears: sequence of
     (w, sw, y, input) with w packed [N][K/2] uint8, sw [N] f32, y [N] f32
     (written), input = -1 for the pass input or the index of an earlier
     linear.  Returns the y tensors."""
-    arr = (ChainLinear * len(linears))()
-    for i, (w, sw, y, inp) in enumerate(linears):
-        N = sw.numel()
-        K = 2 * w.shape[-1] if w.dim() == 2 else 0
-        arr[i] = ChainLinear(_ptr(w), _ptr(sw), _ptr(y), N, K, inp, 0)
+    arr = chain_descriptors(linears)
+    need = raw.w4_chain_workspace_bytes(arr, len(linears), x0.numel())
     if workspace is None:
-        workspace = torch.empty(raw.w4_workspace_bytes(OP_CHAIN_Q4, 1, 1, 1, 0), dtype=torch.uint8,
-                                device=x0.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=x0.device)
     _check(raw.w4_chain_q4(_ptr(x0), x0.numel(), arr, len(linears), passes, pass_output, _ptr(workspace),
                            workspace.numel(), _stream(stream)), "w4_chain_q4")
     return [y for _, _, y, _ in linears]
