@@ -40,8 +40,9 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPF = 8;  // 16-byte weight chunks a lane holds in registers across a barrier
-static_assert(kChainMaxK == 8 * 2 * kThreads, "K <= 8192: at most 8 float2 of the input per thread");
+constexpr int kPF = 8;  // 16-byte weight chunks a lane holds in registers while it waits
+constexpr int kVPerRound = 1024 / (2 * kThreads);  // float2 of the input per thread per 1024 of K
+static_assert(kChainMaxK == 8 * 1024, "K <= 8192: at most 8 rounds of 32 chunks");
 
 struct ChainLin {
     const uint4 *w;  // packed row-major, K/2 bytes per row (16-byte chunks)
@@ -170,7 +171,7 @@ W4_DEV int warp_sum(int v) {
 template <int ROUNDS>
 struct RowsInRegs {
     static constexpr int n = kPF / ROUNDS;
-    static constexpr int value = n >= 8 ? 8 : n >= 4 ? 4 : n >= 2 ? 2 : 1;
+    static constexpr int value = n >= 8 ? 8 : n >= 4 ? 4 : n >= 2 ? 2 : 1;  // at most 8 (lanes 4i hold row i)
 };
 
 // Sums v[i] over the 32 lanes for NR rows at once (NR a power of two <= 8):
@@ -200,8 +201,9 @@ struct Prefetched {
     uint4 w[kPF];
     float sw;
     float *y;
-    uint64_t *t;  // the row's tagged copy, or null
-    int32_t pn;   // the row's index in the pass output, or -1
+    uint64_t *t;    // the row's tagged copy, or null
+    int32_t pn;     // the row's index in the pass output, or -1
+    int32_t nrows;  // rows of the stage this warp owns
 };
 
 // Rows of stage S this warp owns (rows gw, gw + nw, ...).
@@ -214,6 +216,7 @@ W4_DEV void prefetch_stage(const ChainLin *lin, const ChainStage &S, int pass_ou
     constexpr int NR = RowsInRegs<ROUNDS>::value;
     const int Kc = S.K >> 5;
     const int nrows = rows_of_warp(S, gw, nw);
+    pf.nrows = nrows;
     const int lend = S.lin0 + S.nlin;
     int l = S.lin0;
 #pragma unroll
@@ -281,7 +284,7 @@ W4_DEV void compute_stage(const ChainLin *lin, const ChainStage &S, int pass_out
     const int K = S.K, Kc = K >> 5;
     const uint4 *xe4 = reinterpret_cast<const uint4 *>(xs);
     const uint4 *xo4 = reinterpret_cast<const uint4 *>(xs + (K >> 1));
-    const int nrows = rows_of_warp(S, gw, nw);
+    const int nrows = pf.nrows;
     // acc = sum xq*u - 8 * sum xq; each lane subtracts 8x its own chunks' code sum
     int xsum = 0;
 #pragma unroll
@@ -330,6 +333,7 @@ W4_DEV bool wait_pair(const uint64_t *src, uint32_t want, ulonglong2 &a) {
     if (ok()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        __nanosleep(64);  // fewer requests on the lines every CTA polls: measured best of 0-512 ns
         a = ld_relaxed_gpu_v2(src);
         if (ok()) return true;
         if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
@@ -337,8 +341,8 @@ W4_DEV bool wait_pair(const uint64_t *src, uint32_t want, ulonglong2 &a) {
 }
 
 // One stage on this CTA: quantize_row_q8 of the stage's input into shared
-// memory (ROUNDS float2 per thread covers K <= 1024 * ROUNDS), then this
-// warp's rows.  False when a wait for an input element ran out.
+// memory (ROUNDS * kVPerRound float2 per thread covers K <= 1024 * ROUNDS),
+// then this warp's rows.  False when a wait for an input element ran out.
 template <int ROUNDS>
 W4_DEV bool run_stage(const ChainParams &p, const ChainLin *lin, const ChainStage &S, int gs, int pass, int gw,
                       int nw, int warp, int lane, const Prefetched &pf, int8_t *xs, float *red_max, int *fail_flag) {
@@ -357,24 +361,25 @@ W4_DEV bool run_stage(const ChainParams &p, const ChainLin *lin, const ChainStag
         want = (uint32_t)((pass - 1) * p.n_stage + p.s_out + 1);
     }
 
+    constexpr int KV = ROUNDS * kVPerRound;  // float2 of the input per thread
     const int n2 = K >> 1;
-    float2 v[ROUNDS];
+    float2 v[KV];
     if (plain) {
 #pragma unroll
-        for (int u = 0; u < ROUNDS; ++u) {
+        for (int u = 0; u < KV; ++u) {
             const int j = threadIdx.x + u * kThreads;
             v[u] = j < n2 ? __ldg(reinterpret_cast<const float2 *>(plain) + j) : make_float2(0.f, 0.f);
         }
     } else {
-        ulonglong2 a[ROUNDS];
+        ulonglong2 a[KV];
 #pragma unroll
-        for (int u = 0; u < ROUNDS; ++u) {
+        for (int u = 0; u < KV; ++u) {
             const int j = threadIdx.x + u * kThreads;
             a[u] = j < n2 ? ld_relaxed_gpu_v2(tin + 2 * j) : make_ulonglong2(0, 0);
         }
         bool good = true;
 #pragma unroll
-        for (int u = 0; u < ROUNDS; ++u) {
+        for (int u = 0; u < KV; ++u) {
             const int j = threadIdx.x + u * kThreads;
             if (j < n2) good = good && wait_pair(tin + 2 * j, want, a[u]);
             v[u] = make_float2(__uint_as_float((uint32_t)a[u].x), __uint_as_float((uint32_t)a[u].y));
@@ -386,7 +391,7 @@ W4_DEV bool run_stage(const ChainParams &p, const ChainLin *lin, const ChainStag
     }
     float amax = 0.0f;
 #pragma unroll
-    for (int u = 0; u < ROUNDS; ++u) amax = fmaxf(amax, fmaxf(fabsf(v[u].x), fabsf(v[u].y)));
+    for (int u = 0; u < KV; ++u) amax = fmaxf(amax, fmaxf(fabsf(v[u].x), fabsf(v[u].y)));
 #pragma unroll
     for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     if (lane == 0) red_max[warp] = amax;
@@ -399,7 +404,7 @@ W4_DEV bool run_stage(const ChainParams &p, const ChainLin *lin, const ChainStag
     const float r = sx != 0.0f ? __frcp_rn(sx) : 0.0f;
     const bool fast = isfinite(r);
 #pragma unroll
-    for (int u = 0; u < ROUNDS; ++u) {
+    for (int u = 0; u < KV; ++u) {
         const int j = threadIdx.x + u * kThreads;
         if (j < n2) {
             int c0 = 0, c1 = 0;
@@ -629,3 +634,4 @@ int chain_plan_launch(const float *x0, int32_t K0, const w4_chain_linear *lin, i
 }
 
 }  // namespace w4
+
