@@ -245,6 +245,208 @@ W4_DEV void unit_mma(const uint8_t *w0, const uint8_t *w8, int c0, int g, int t,
     }
 }
 
+// W4A16 scales of rows [row0, row0 + rows) x units [u0, u0 + nun): 16-byte
+// vectors into registers when the rows allow it (stored to shared memory as
+// f32 after the PDL wait by store_scales), otherwise converted straight into
+// shared memory.  Returns whether the vector path was taken.
+template <int KIND>
+W4_DEV bool prefetch_scales(const GemvParams &p, int row0, int rows, int u0, int nun, int nthr, uint4 (&sv)[2],
+                            uint8_t *smem) {
+    constexpr int kMaxSc = 2;
+    const int tid = threadIdx.x;
+    bool svec = false;
+    const int spr = nun >> 3;  // 16-byte scale vectors per row
+    svec = (KIND == KIND_W4A16) && p.s_vec && rows * spr <= kMaxSc * nthr;
+    const uint32_t spr_magic = div_magic((uint32_t)max(spr, 1));
+    if constexpr (KIND == KIND_W4A16) {
+        const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
+        if (svec) {
+#pragma unroll
+            for (int i = 0; i < kMaxSc; ++i) {
+                const int j = tid + i * nthr;
+                if (j < rows * spr) {
+                    const int r = fast_div(j, spr_magic);
+                    sv[i] = __ldg(reinterpret_cast<const uint4 *>(s16 + (size_t)(row0 + r) * p.ng + u0) + (j - r * spr));
+                }
+            }
+        } else {
+            const uint32_t nun_magic = div_magic((uint32_t)nun);
+            float *scf = reinterpret_cast<float *>(smem + p.sc_off);
+            for (int i = tid; i < rows * nun; i += nthr) {
+                const int r = fast_div(i, nun_magic), gi = i - r * nun;
+                scf[r * p.sstride + gi] = __half2float(__ushort_as_half(__ldg(s16 + (size_t)(row0 + r) * p.ng + u0 + gi)));
+            }
+        }
+    }
+
+    return svec;
+}
+
+// Activations of columns [k0, k0 + span_k) into shared memory: each group
+// of 8 columns becomes four 16-bit pairs in the order of the weight pairs
+// (zero beyond K): W4A16 bf16 (x0 x4)(x1 x5)(x2 x6)(x3 x7); W4A8 the same as
+// exact f16; W8A8 f16 (x0 x1)(x2 x3)(x4 x5)(x6 x7).
+template <int KIND>
+W4_DEV void stage_x(const GemvParams &p, int k0, int span_k, int nthr, uint8_t *smem) {
+    constexpr bool kInt = KIND != KIND_W4A16;
+    const int tid = threadIdx.x;
+    {
+        const int per_row = span_k >> 3;  // 8-element groups
+        const uint32_t pr_magic = div_magic((uint32_t)per_row);
+        for (int j = tid; j < p.M * per_row; j += nthr) {
+            const int m = fast_div(j, pr_magic), b8 = j - m * per_row;
+            const int kk = k0 + 8 * b8;
+            uint4 o;
+            if constexpr (kInt) {
+                const int8_t *xr = static_cast<const int8_t *>(p.x) + (size_t)m * p.K;
+                uint2 v;
+                if (p.x_vec && kk + 8 <= p.K) {
+                    v = __ldg(reinterpret_cast<const uint2 *>(xr + kk));
+                } else {
+                    uint32_t lo = 0, hi = 0;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint32_t b = (kk + i < p.K) ? (uint32_t)(uint8_t)xr[kk + i] : 0u;
+                        if (i < 4) lo |= b << (8 * i);
+                        else hi |= b << (8 * (i - 4));
+                    }
+                    v = make_uint2(lo, hi);
+                }
+                const uint32_t xsel4[4] = {0x0400u, 0x0501u, 0x0602u, 0x0703u};
+                const uint32_t xsel8[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
+                uint32_t b[4];
+                s8_to_f16_pairs(v.x, v.y, (KIND == KIND_W4A8) ? xsel4 : xsel8, b);
+                o = make_uint4(b[0], b[1], b[2], b[3]);
+            } else {
+                const uint16_t *xr = static_cast<const uint16_t *>(p.x) + (size_t)m * p.K;
+                uint4 v;
+                if (p.x_vec && kk + 8 <= p.K) {
+                    v = __ldg(reinterpret_cast<const uint4 *>(xr + kk));
+                } else {
+                    uint32_t e[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) e[i] = (kk + i < p.K) ? (uint32_t)xr[kk + i] : 0u;
+                    v = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+                }
+                o = make_uint4(prmt(v.x, v.z, 0x5410), prmt(v.x, v.z, 0x7632), prmt(v.y, v.w, 0x5410),
+                               prmt(v.y, v.w, 0x7632));
+            }
+            *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) = o;
+        }
+    }
+
+}
+
+// Second half of prefetch_scales: the vector path's registers -> f32 in shared memory.
+template <int KIND>
+W4_DEV void store_scales(const GemvParams &p, int rows, int nun, int nthr, bool svec, const uint4 (&sv)[2],
+                         uint8_t *smem) {
+    constexpr int kMaxSc = 2;
+    const int tid = threadIdx.x;
+    const int spr = nun >> 3;
+    const uint32_t spr_magic = div_magic((uint32_t)max(spr, 1));
+    if constexpr (KIND == KIND_W4A16) {
+        if (svec) {
+            float *scf = reinterpret_cast<float *>(smem + p.sc_off);
+#pragma unroll
+            for (int i = 0; i < kMaxSc; ++i) {
+                const int j = tid + i * nthr;
+                if (j < rows * spr) {
+                    const int r = fast_div(j, spr_magic), c8 = j - r * spr;
+                    const uint32_t w4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        scf[r * p.sstride + 8 * c8 + e] =
+                            __half2float(__ushort_as_half((unsigned short)(w4[e >> 1] >> (16 * (e & 1)))));
+                }
+            }
+        }
+    }
+}
+
+// Combines the K-split warps in index order, then the cluster's K splits in
+// rank order (distributed shared memory), and writes y (rank 0, K-warp 0).
+template <int KIND, int RB, int MT, typename Acc>
+W4_DEV void combine_and_store(const GemvParams &p, Acc (&acc)[MT][4], int wr, int wk, int lane, int g, int t,
+                              int rowbase, uint8_t *smem) {
+    constexpr bool kInt = KIND != KIND_W4A16;
+    // ---- 5. combine the K-split warps in index order.
+    uint32_t *red = reinterpret_cast<uint32_t *>(smem + p.red_off);
+    constexpr int kVals = MT * 4;
+    const int WK = p.WK;
+    if (WK > 1) {
+        if (wk > 0) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    red[((wk * p.WR + wr) * 32 + lane) * kVals + mt * 4 + i] = kInt ? (uint32_t)acc[mt][i]
+                                                                                  : __float_as_uint((float)acc[mt][i]);
+        }
+        __syncthreads();
+        if (wk == 0) {
+            for (int w2 = 1; w2 < WK; ++w2)
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t v = red[((w2 * p.WR + wr) * 32 + lane) * kVals + mt * 4 + i];
+                        if constexpr (kInt) acc[mt][i] += (int)v;
+                        else acc[mt][i] += __uint_as_float(v);
+                    }
+        }
+    }
+
+    // ---- combine the cluster's K splits in rank order (distributed shared memory).
+    const int S = gridDim.y;
+    if (S > 1) {
+        __syncthreads();  // red is reused below
+        if (wk == 0) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    red[(wr * 32 + lane) * kVals + mt * 4 + i] = kInt ? (uint32_t)acc[mt][i]
+                                                                     : __float_as_uint((float)acc[mt][i]);
+        }
+        cluster_sync();
+        if (blockIdx.y == 0 && wk == 0) {
+            for (int r = 1; r < S; ++r) {
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t v =
+                            dsmem_ld_u32(dsmem_map(&red[(wr * 32 + lane) * kVals + mt * 4 + i], (uint32_t)r));
+                        if constexpr (kInt) acc[mt][i] += (int)v;
+                        else acc[mt][i] += __uint_as_float(v);
+                    }
+            }
+        }
+        cluster_sync();  // peers keep their shared memory alive until rank 0 has read it
+    }
+
+    // ---- epilogue.
+    if (blockIdx.y != 0 || wk != 0) return;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (RB == 8 && i >= 2) continue;
+            const int m = 8 * mt + 2 * t + (i & 1);
+            const int n = rowbase + g + 8 * (i >> 1);
+            if (m >= p.M || n >= p.N) continue;
+            float out;
+            if constexpr (kInt) {
+                const float sw = static_cast<const float *>(p.scale)[n];
+                out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[mt][i]), p.sx[m]), sw);
+            } else {
+                out = (float)acc[mt][i];
+            }
+            p.y[(size_t)m * p.N + n] = out;
+        }
+}
+
 // ---------------------------------------------------------------- kernel
 //
 // One CTA: rows [row0, row0 + R) x the K range of split blockIdx.y.
@@ -304,84 +506,13 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
             }
         }
     }
-    // W4A16 scales: 16-byte vectors when the rows allow it, converted to f32
-    // after the wait; otherwise a plain loop (odd shapes).
     constexpr int kMaxSc = 2;
     uint4 sv[kMaxSc];
-    const int spr = nun >> 3;  // 16-byte scale vectors per row
-    const bool svec = (KIND == KIND_W4A16) && p.s_vec && rows * spr <= kMaxSc * nthr;
-    const uint32_t spr_magic = div_magic((uint32_t)max(spr, 1));
-    if constexpr (KIND == KIND_W4A16) {
-        const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
-        if (svec) {
-#pragma unroll
-            for (int i = 0; i < kMaxSc; ++i) {
-                const int j = tid + i * nthr;
-                if (j < rows * spr) {
-                    const int r = fast_div(j, spr_magic);
-                    sv[i] = __ldg(reinterpret_cast<const uint4 *>(s16 + (size_t)(row0 + r) * p.ng + u0) + (j - r * spr));
-                }
-            }
-        } else {
-            const uint32_t nun_magic = div_magic((uint32_t)nun);
-            float *scf = reinterpret_cast<float *>(smem + p.sc_off);
-            for (int i = tid; i < rows * nun; i += nthr) {
-                const int r = fast_div(i, nun_magic), gi = i - r * nun;
-                scf[r * p.sstride + gi] = __half2float(__ushort_as_half(__ldg(s16 + (size_t)(row0 + r) * p.ng + u0 + gi)));
-            }
-        }
-    }
+    const bool svec = prefetch_scales<KIND>(p, row0, rows, u0, nun, nthr, sv, smem);
 
     griddep_wait();  // x may be written, and y read, by the previous kernel
 
-    // ---- 2. activations: each group of 8 columns becomes four 16-bit pairs
-    // in the order of the weight pairs (zero beyond K):
-    //   W4A16 bf16 (x0 x4)(x1 x5)(x2 x6)(x3 x7); W4A8 the same as exact f16;
-    //   W8A8 f16 (x0 x1)(x2 x3)(x4 x5)(x6 x7).
-    {
-        const int per_row = span_k >> 3;  // 8-element groups
-        const uint32_t pr_magic = div_magic((uint32_t)per_row);
-        for (int j = tid; j < p.M * per_row; j += nthr) {
-            const int m = fast_div(j, pr_magic), b8 = j - m * per_row;
-            const int kk = k0 + 8 * b8;
-            uint4 o;
-            if constexpr (kInt) {
-                const int8_t *xr = static_cast<const int8_t *>(p.x) + (size_t)m * p.K;
-                uint2 v;
-                if (p.x_vec && kk + 8 <= p.K) {
-                    v = __ldg(reinterpret_cast<const uint2 *>(xr + kk));
-                } else {
-                    uint32_t lo = 0, hi = 0;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const uint32_t b = (kk + i < p.K) ? (uint32_t)(uint8_t)xr[kk + i] : 0u;
-                        if (i < 4) lo |= b << (8 * i);
-                        else hi |= b << (8 * (i - 4));
-                    }
-                    v = make_uint2(lo, hi);
-                }
-                const uint32_t xsel4[4] = {0x0400u, 0x0501u, 0x0602u, 0x0703u};
-                const uint32_t xsel8[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
-                uint32_t b[4];
-                s8_to_f16_pairs(v.x, v.y, (KIND == KIND_W4A8) ? xsel4 : xsel8, b);
-                o = make_uint4(b[0], b[1], b[2], b[3]);
-            } else {
-                const uint16_t *xr = static_cast<const uint16_t *>(p.x) + (size_t)m * p.K;
-                uint4 v;
-                if (p.x_vec && kk + 8 <= p.K) {
-                    v = __ldg(reinterpret_cast<const uint4 *>(xr + kk));
-                } else {
-                    uint32_t e[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) e[i] = (kk + i < p.K) ? (uint32_t)xr[kk + i] : 0u;
-                    v = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
-                }
-                o = make_uint4(prmt(v.x, v.z, 0x5410), prmt(v.x, v.z, 0x7632), prmt(v.y, v.w, 0x5410),
-                               prmt(v.y, v.w, 0x7632));
-            }
-            *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) = o;
-        }
-    }
+    stage_x<KIND>(p, k0, span_k, nthr, smem);
 
     // ---- 3. weight tile into shared memory (further rounds for big tiles).
     for (int base = 0; base < wchunks; base += kMaxLd * nthr) {
@@ -415,23 +546,7 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
             }
         }
     }
-    if constexpr (KIND == KIND_W4A16) {
-        if (svec) {
-            float *scf = reinterpret_cast<float *>(smem + p.sc_off);
-#pragma unroll
-            for (int i = 0; i < kMaxSc; ++i) {
-                const int j = tid + i * nthr;
-                if (j < rows * spr) {
-                    const int r = fast_div(j, spr_magic), c8 = j - r * spr;
-                    const uint32_t w4[4] = {sv[i].x, sv[i].y, sv[i].z, sv[i].w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        scf[r * p.sstride + 8 * c8 + e] =
-                            __half2float(__ushort_as_half((unsigned short)(w4[e >> 1] >> (16 * (e & 1)))));
-                }
-            }
-        }
-    }
+    store_scales<KIND>(p, rows, nun, nthr, svec, sv, smem);
     __syncthreads();
     // Let the next kernel on the stream start (and begin its weight fetch)
     // once this CTA's tiles are in shared memory.
@@ -534,80 +649,142 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
         if constexpr (N64) __syncthreads();  // the next phase overwrites the tile
     }
 
-    // ---- 5. combine the K-split warps in index order.
-    uint32_t *red = reinterpret_cast<uint32_t *>(smem + p.red_off);
-    constexpr int kVals = MT * 4;
-    if (WK > 1) {
-        if (wk > 0) {
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    red[((wk * p.WR + wr) * 32 + lane) * kVals + mt * 4 + i] = kInt ? (uint32_t)acc[mt][i]
-                                                                                  : __float_as_uint((float)acc[mt][i]);
-        }
-        __syncthreads();
-        if (wk == 0) {
-            for (int w2 = 1; w2 < WK; ++w2)
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t v = red[((w2 * p.WR + wr) * 32 + lane) * kVals + mt * 4 + i];
-                        if constexpr (kInt) acc[mt][i] += (int)v;
-                        else acc[mt][i] += __uint_as_float(v);
-                    }
-        }
-    }
+    combine_and_store<KIND, RB, MT>(p, acc, wr, wk, lane, g, t, row0 + rbase, smem);
+}
 
-    // ---- combine the cluster's K splits in rank order (distributed shared memory).
-    const int S = gridDim.y;
-    if (S > 1) {
-        __syncthreads();  // red is reused below
-        if (wk == 0) {
+// ---------------------------------------------------------------- direct-load kernel
+//
+// gemv_kernel's arithmetic on the row-major layout -- the same unit -> warp
+// assignment, MMA operand order, fold order and K-split combine -- with each
+// thread's A fragments loaded straight from global memory into registers
+// (one 32-bit word per row per 32-column chunk, issued before the PDL wait)
+// instead of through a shared-memory weight tile.  Only activations and
+// W4A16 scales pass through shared memory, so there is no tile to store,
+// re-read and synchronise on.  Results are bit-identical to gemv_kernel, and
+// so to the interleaved layout and across M.
+template <int KIND, int RB, int MT, int CPG, int NW>
+__global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant__ GemvParams p) {
+    static_assert(KIND != KIND_W8A8 && NW % CPG == 0, "int4 kinds, whole units per window");
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wr = warp % p.WR, wk = warp / p.WR;
+    const int g = lane >> 2, t = lane & 3;
+    const int row0 = blockIdx.x * p.R;
+    const int u0 = blockIdx.y * p.upc;
+    const int nun = min(p.units, u0 + p.upc) - u0;  // >= 1 (host guarantees)
+    const int k0 = u0 * p.unit_k;
+    const int span_k = nun * p.unit_k;
+    constexpr bool kInt = KIND != KIND_W4A16;
+    const int rows = min(p.R, p.N - row0);
+    const int nthr = blockDim.x;
+    const int WK = p.WK;
+    const int rbase = wr * RB;
+    // the warp's units: wk, wk + WK, ... of the CTA's span (gemv_kernel's order)
+    const int nu_w = wk < nun ? (nun - wk + WK - 1) / WK : 0;
+    constexpr int kUW = NW / CPG;  // units held in registers per window
+    // rows g and g + 8 of the warp's block, clamped to a valid row (clamped rows are never stored)
+    const int rA = min(row0 + rbase + g, p.N - 1);
+    const int rB = min(row0 + rbase + g + 8, p.N - 1);
+    const uint8_t *wA = p.w + (size_t)rA * p.Kb + (size_t)u0 * p.unit_bytes + 4 * t;
+    const uint8_t *wB = p.w + (size_t)rB * p.Kb + (size_t)u0 * p.unit_bytes + 4 * t;
+    uint32_t fa[NW], fb[NW];
+    // words of units jw .. jw + kUW - 1 of the warp (chunk cc of unit j at byte 16 * cc)
+    auto load_window = [&](int jw) {
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt)
+        for (int j = 0; j < kUW; ++j) {
+            if (jw + j < nu_w) {
+                const size_t off = (size_t)(wk + (jw + j) * WK) * p.unit_bytes;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    red[(wr * 32 + lane) * kVals + mt * 4 + i] = kInt ? (uint32_t)acc[mt][i]
-                                                                     : __float_as_uint((float)acc[mt][i]);
-        }
-        cluster_sync();
-        if (blockIdx.y == 0 && wk == 0) {
-            for (int r = 1; r < S; ++r) {
-#pragma unroll
-                for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const uint32_t v =
-                            dsmem_ld_u32(dsmem_map(&red[(wr * 32 + lane) * kVals + mt * 4 + i], (uint32_t)r));
-                        if constexpr (kInt) acc[mt][i] += (int)v;
-                        else acc[mt][i] += __uint_as_float(v);
-                    }
+                for (int cc = 0; cc < CPG; ++cc) {
+                    fa[j * CPG + cc] = __ldg(reinterpret_cast<const uint32_t *>(wA + off + 16 * cc));
+                    if (RB == 16) fb[j * CPG + cc] = __ldg(reinterpret_cast<const uint32_t *>(wB + off + 16 * cc));
+                }
             }
         }
-        cluster_sync();  // peers keep their shared memory alive until rank 0 has read it
-    }
+    };
+    load_window(0);
+    constexpr int kMaxSc = 2;
+    uint4 sv[kMaxSc];
+    const bool svec = prefetch_scales<KIND>(p, row0, rows, u0, nun, nthr, sv, smem);
 
-    // ---- epilogue.
-    if (blockIdx.y != 0 || wk != 0) return;
+    griddep_wait();  // x may be written, and y read, by the previous kernel
+    stage_x<KIND>(p, k0, span_k, nthr, smem);
+    store_scales<KIND>(p, rows, nun, nthr, svec, sv, smem);
+    __syncthreads();
+    griddep_launch_dependents();
+
+    using Acc = typename std::conditional<kInt, int, float>::type;
+    Acc acc[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (RB == 8 && i >= 2) continue;
-            const int m = 8 * mt + 2 * t + (i & 1);
-            const int n = row0 + rbase + g + 8 * (i >> 1);
-            if (m >= p.M || n >= p.N) continue;
-            float out;
-            if constexpr (kInt) {
-                const float sw = static_cast<const float *>(p.scale)[n];
-                out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[mt][i]), p.sx[m]), sw);
-            } else {
-                out = (float)acc[mt][i];
+        for (int i = 0; i < 4; ++i) acc[mt][i] = 0;
+    const uint8_t *xrow[MT];
+    bool xvalid[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int m = g + 8 * mt;
+        xvalid[mt] = m < p.M;
+        xrow[mt] = smem + p.x_off + (xvalid[mt] ? m : 0) * p.xstride + 16 * t;
+    }
+    const float *scf = reinterpret_cast<const float *>(smem + p.sc_off);
+    const float *sc0 = scf + (rbase + g) * p.sstride;
+    const float *sc1 = scf + (rbase + g + 8) * p.sstride;
+
+    for (int jw = 0; jw < nu_w; jw += kUW) {
+        if (jw > 0) load_window(jw);
+#pragma unroll
+        for (int j = 0; j < kUW; ++j) {
+            if (jw + j < nu_w) {
+                const int u = wk + (jw + j) * WK;  // unit, relative to the CTA's span
+                float part[MT][4];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) part[mt][i] = 0.0f;
+#pragma unroll
+                for (int cc = 0; cc < CPG; ++cc) {
+                    uint32_t pa[4], pb[4] = {0u, 0u, 0u, 0u};
+                    if constexpr (KIND == KIND_W4A16) {
+                        unpack_signed_bf16(fa[j * CPG + cc], pa);
+                        if (RB == 16) unpack_signed_bf16(fb[j * CPG + cc], pb);
+                    } else {
+                        unpack_biased_f16(fa[j * CPG + cc], pa);
+                        if (RB == 16) unpack_biased_f16(fb[j * CPG + cc], pb);
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+                        if (xvalid[mt]) xv = *reinterpret_cast<const uint4 *>(xrow[mt] + 64 * (CPG * u + cc));
+                        if constexpr (KIND == KIND_W4A16) {
+                            mma_bf16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
+                            mma_bf16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+                        } else {
+                            mma_f16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
+                            mma_f16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+                        }
+                    }
+                }
+                if constexpr (KIND == KIND_W4A16) {
+                    const float s0 = sc0[u];
+                    const float s1 = (RB == 16) ? sc1[u] : 0.0f;
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) {
+                        acc[mt][0] = fmaf(s0, part[mt][0], acc[mt][0]);
+                        acc[mt][1] = fmaf(s0, part[mt][1], acc[mt][1]);
+                        acc[mt][2] = fmaf(s1, part[mt][2], acc[mt][2]);
+                        acc[mt][3] = fmaf(s1, part[mt][3], acc[mt][3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) acc[mt][i] += __float2int_rn(part[mt][i]);
+                }
             }
-            p.y[(size_t)m * p.N + n] = out;
         }
+    }
+    combine_and_store<KIND, RB, MT>(p, acc, wr, wk, lane, g, t, row0 + rbase, smem);
 }
 
 // ---------------------------------------------------------------- generic fallback
@@ -702,6 +879,51 @@ cudaError_t launch_one(const GemvParams &p, int S, int threads, int smem, cudaSt
     return cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, N64, RB, MT, CPG>, p);
 }
 
+constexpr int kDirectWords = 16;  // words per row a thread holds (gemv_direct_kernel NW)
+
+template <int KIND, int RB, int MT, int CPG>
+cudaError_t launch_direct(const GemvParams &p, int S, int threads, int smem, cudaStream_t st, bool pdl) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    auto *kern = gemv_direct_kernel<KIND, RB, MT, CPG, kDirectWords>;
+    std::call_once(once, [kern] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(p.N, p.R), (unsigned)S, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    if (S > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = 1;
+        attrs[na].val.clusterDim.y = (unsigned)S;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = (unsigned)na;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int KIND, int CPG>
+cudaError_t dispatch_direct(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
+    if (s.RB == 8) {
+        if (s.MT == 1) return launch_direct<KIND, 8, 1, CPG>(p, s.S, threads, smem, st, pdl);
+        return launch_direct<KIND, 8, 2, CPG>(p, s.S, threads, smem, st, pdl);
+    }
+    if (s.MT == 1) return launch_direct<KIND, 16, 1, CPG>(p, s.S, threads, smem, st, pdl);
+    return launch_direct<KIND, 16, 2, CPG>(p, s.S, threads, smem, st, pdl);
+}
+
 template <int KIND, bool N64, int CPG>
 cudaError_t dispatch_rb_mt(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
     if (s.RB == 8) {
@@ -745,7 +967,7 @@ bool geometry(const LinearArgs &a, GemvParams &p) {
 int pad_to(int bytes, int target) { return bytes + ((target - bytes % 128) + 256) % 128; }
 
 // Shared-memory carve-up for a given shape (p.upc, p.upp set); returns total bytes.
-int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p) {
+int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_tile = true) {
     const bool n64 = a.layout == W4_LAYOUT_N64;
     p.R = n64 ? 64 : s.RB * s.WR;
     p.WR = n64 ? 64 / s.RB : s.WR;
@@ -759,7 +981,7 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p) {
     p.raw_off = off;
     if (n64) off += (int)round_up((int64_t)span_k * 32, 128);
     p.w_off = off;
-    off += (int)round_up((int64_t)p.R * p.wstride, 128);
+    if (weight_tile) off += (int)round_up((int64_t)p.R * p.wstride, 128);
     p.x_off = off;
     off += (int)round_up((int64_t)a.M * p.xstride, 128);
     p.sc_off = off;
@@ -850,6 +1072,21 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     s.S = S;
     const int threads = 32 * p.WR * p.WK;
     const bool pdl = (a.flags & W4_FLAG_PDL) != 0;
+    // Row-major int4 with two activation tiles (M > 8): fragments straight
+    // from global memory, so shared memory holds only x and the scales and
+    // more CTAs fit per SM (the same arithmetic, so the same bits).  For
+    // M <= 8 the 128-bit staged tile streams HBM better.
+    if (!n64 && a.M > 8 && a.kind != KIND_W8A8 && (p.cpg == 1 || p.cpg == 2 || p.cpg == 4) &&
+        (a.kind == KIND_W4A16 || p.cpg == 1)) {
+        GemvParams q = p;
+        const int dsmem = plan_smem(a, s, q, false);
+        if (a.kind == KIND_W4A8) return dispatch_direct<KIND_W4A8, 1>(q, s, threads, dsmem, st, pdl);
+        switch (p.cpg) {
+            case 1: return dispatch_direct<KIND_W4A16, 1>(q, s, threads, dsmem, st, pdl);
+            case 2: return dispatch_direct<KIND_W4A16, 2>(q, s, threads, dsmem, st, pdl);
+            default: return dispatch_direct<KIND_W4A16, 4>(q, s, threads, dsmem, st, pdl);
+        }
+    }
     switch (a.kind) {
         case KIND_W4A8:
             return n64 ? dispatch_rb_mt<KIND_W4A8, true, 1>(p, s, threads, smem, st, pdl)
