@@ -79,8 +79,6 @@ WORKLOADS = {
 # capture (profiles/); None where no capture matches the current kernel.
 TRAFFIC = {
     "w4a16_gemv_m1": 2395392,                 # profiles/gemv_w4a16_m1_n2048_k2048.md
-    "w4a8_prefill_m2048_n13312": 72658944,    # profiles/gemm_prefill_m2048_n13312_k2048.md
-    "w4a16_prefill_m2048_n13312": 72578816,   # profiles/gemm_prefill_m2048_n13312_k2048.md
 }
 
 

@@ -2,18 +2,23 @@
 //
 // y[m][n] = sum_k x[m][k] W[n][k], W never stored in float in global memory.
 //
-// Per CTA: a 128 (output channels n) x 256 (activation rows m) tile of y,
-// accumulated in tensor memory over K in steps of 64 columns:
-//   warp 0      TMA producer: the packed weight tile [128 rows][32|64 B] and
-//               the 16-bit activation tile [256 rows][64] (128-byte swizzle)
-//               of each stage, both on one transaction-count mbarrier;
-//   warp 1      allocates 256 TMEM columns and issues tcgen05.mma (one
-//               thread): kind::f16, A = weights (M = 128), B = activations
-//               (N = 256), K-major shared-memory descriptors, f32 accumulator;
-//               tcgen05.commit releases each stage and finally the tile;
-//   warps 2-9   convert the packed weights of a stage into the A operand tile
-//               (128B-swizzled, K-major) and later run the epilogue:
-//               tcgen05.ld of the accumulator, scales, coalesced stores.
+// Persistent: one CTA per SM walks the 128 (output channels n) x 256
+// (activation rows m) tiles of y (n fastest, so concurrent CTAs share the
+// activation tiles in L2), accumulating each in tensor memory over K in steps
+// of 64 columns; the stage pipeline runs on across tile boundaries:
+//   warp 0       TMA producer: the packed weight tile [128 rows][32|64 B] and
+//                the 16-bit activation tile [256 rows][64] (128-byte swizzle)
+//                of each stage, both on one transaction-count mbarrier;
+//   warp 1       allocates 512 TMEM columns (two 256-column accumulators) and
+//                issues tcgen05.mma (one thread): kind::f16, A = weights
+//                (M = 128), B = activations (N = 256), K-major shared-memory
+//                descriptors, f32 accumulator; tcgen05.commit releases each
+//                stage, and each finished tile's accumulator;
+//   warps 2-9    convert the packed weights of a stage into the A operand tile
+//                (128B-swizzled, K-major);
+//   warps 10-17  epilogue of tile i (tcgen05.ld of the accumulator, scales,
+//                coalesced stores) while the MMA warp accumulates tile i + 1
+//                into the other accumulator.
 // Weight conversion (the dequantisation happens only in shared memory):
 //   W4A16  w = bf16_rne(f32(q) * f32(s)): q * s is exact in f32 and rounded
 //          once to bf16 ("Fused int4 ..." sections 2.2-2.3 dequantised once per
@@ -50,8 +55,9 @@ constexpr int kBN = 256;   // activation rows per tile (UMMA N)
 constexpr int kBK = 64;    // columns per stage (128 bytes of 16-bit values)
 constexpr int kStages = 4;
 constexpr int kConvWarps = 8;
-constexpr int kThreads = 64 + 32 * kConvWarps;
-constexpr int kTmemCols = 256;
+constexpr int kEpiWarps = 8;  // two per TMEM lane quadrant, one per column half
+constexpr int kThreads = 64 + 32 * (kConvWarps + kEpiWarps);
+constexpr int kTmemCols = 512;  // two accumulators of kBN columns
 
 struct GemmParams {
     CUtensorMap xmap;  // 16-bit activations [M][Kx], box {64, 256}, 128B swizzle
@@ -62,14 +68,17 @@ struct GemmParams {
     float *y;                // [M][N]
     uint32_t *status;
     int M, N, K, G, ng;
-    int nk;  // k-blocks of 64 columns
+    int nk;   // k-blocks of 64 columns
+    int ntn;  // tiles along N (n fastest)
+    int ntiles;
 };
 
 struct Smem {
     uint64_t tma_full[kStages];
     uint64_t conv_full[kStages];
     uint64_t empty[kStages];
-    uint64_t acc_full;
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
 };
@@ -218,8 +227,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint8_t *p_tiles = b_tiles + kStages * kBTile;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int m0 = blockIdx.x * kBN;  // activation rows
-    const int n0 = blockIdx.y * kBM;  // weight rows
+    // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...; tile t -> (n-tile t % ntn, m-tile t / ntn)
+    const int my_tiles = blockIdx.x < (unsigned)p.ntiles ? (p.ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto tile_of = [&](int i, int &m0, int &n0) {
+        const int t = (int)blockIdx.x + i * (int)gridDim.x;
+        n0 = (t % p.ntn) * kBM;
+        m0 = (t / p.ntn) * kBN;
+    };
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -227,7 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_init(&sh->conv_full[s], 32 * kConvWarps);
             mbar_init(&sh->empty[s], 1);
         }
-        mbar_init(&sh->acc_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sh->acc_full[b], 1);
+            mbar_init(&sh->acc_empty[b], kEpiWarps);
+        }
         sh->abort = 0;
         fence_mbar_init();
     }
@@ -236,13 +253,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh->tmem_base;
+    const int total = my_tiles * p.nk;  // stages this CTA runs (the pipeline spans tiles)
 
     if (warp == 0) {
         // ---------------- TMA producer
         if (lane == 0) {
-            for (int kb = 0; kb < p.nk; ++kb) {
-                const int s = kb % kStages;
-                if (kb >= kStages && !wait_or_abort(&sh->empty[s], ((kb / kStages) - 1) & 1, sh, p.status)) break;
+            for (int g = 0; g < total; ++g) {
+                const int s = g % kStages, kb = g % p.nk;
+                int m0, n0;
+                tile_of(g / p.nk, m0, n0);
+                if (g >= kStages && !wait_or_abort(&sh->empty[s], ((g / kStages) - 1) & 1, sh, p.status)) break;
                 mbar_arrive_expect_tx(&sh->tma_full[s], kStageTx);
                 tma_load_2d(b_tiles + s * kBTile, &p.xmap, kb * kBK, m0, &sh->tma_full[s]);
                 tma_load_2d(p_tiles + s * kPTile, &p.wmap, kb * kPRow, n0, &sh->tma_full[s]);
@@ -252,52 +272,78 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // ---------------- MMA issuer
         if (lane == 0) {
             bool ok = true;
-            for (int kb = 0; kb < p.nk && ok; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t ph = (kb / kStages) & 1;
-                ok = wait_or_abort(&sh->tma_full[s], ph, sh, p.status) &&
-                     wait_or_abort(&sh->conv_full[s], ph, sh, p.status);
+            int g = 0;
+            for (int i = 0; i < my_tiles && ok; ++i) {
+                const int b = i & 1;
+                if (i >= 2) ok = wait_or_abort(&sh->acc_empty[b], ((i >> 1) - 1) & 1, sh, p.status);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t a_addr = smem_u32(a_tiles + s * kATile);
-                const uint32_t b_addr = smem_u32(b_tiles + s * kBTile);
+                const uint32_t acc = tmem + (uint32_t)(kBN * b);
+                for (int kb = 0; kb < p.nk; ++kb, ++g) {
+                    const int s = g % kStages;
+                    const uint32_t ph = (g / kStages) & 1;
+                    ok = wait_or_abort(&sh->tma_full[s], ph, sh, p.status) &&
+                         wait_or_abort(&sh->conv_full[s], ph, sh, p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(a_tiles + s * kATile);
+                    const uint32_t b_addr = smem_u32(b_tiles + s * kBTile);
 #pragma unroll
-                for (int j = 0; j < kBK / 16; ++j)  // 16 columns (32 bytes) per MMA
-                    umma_f16(tmem, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), kIdesc,
-                             (kb > 0 || j > 0) ? 1u : 0u);
-                umma_commit(&sh->empty[s]);
+                    for (int j = 0; j < kBK / 16; ++j)  // 16 columns (32 bytes) per MMA
+                        umma_f16(acc, smem_desc_sw128(a_addr + 32 * j), smem_desc_sw128(b_addr + 32 * j), kIdesc,
+                                 (kb > 0 || j > 0) ? 1u : 0u);
+                    umma_commit(&sh->empty[s]);
+                }
+                if (ok) umma_commit(&sh->acc_full[b]);
             }
-            if (ok) umma_commit(&sh->acc_full);
         }
-    } else {
-        // ---------------- weight conversion (warps 2..9: 256 threads)
+    } else if (warp < 2 + kConvWarps) {
+        // ---------------- weight conversion (256 threads)
         const int ct = tid - 64;
         const int row = ct & (kBM - 1), half = ct >> 7;  // row of the tile, columns [32 half, 32 half + 32)
-        const int n = n0 + row;
         const int rr = row & 7;
         uint8_t *a_row = a_tiles + (row >> 3) * 1024 + rr * 128;
-        // W4A16 group scales of this thread's 4 chunks, fetched one stage ahead
+        // W4A16 group scales of this thread's 4 chunks, fetched one stage
+        // ahead.  The chunks of a thread share a group when G >= 32 and
+        // consecutive stages share it when G > 64: each distinct scale is
+        // loaded once (these row-strided loads cost a sector lookup per lane).
         float sc_cur[4] = {0.f, 0.f, 0.f, 0.f}, sc_nxt[4] = {0.f, 0.f, 0.f, 0.f};
-        auto load_scales = [&](int kb, float (&dst)[4]) {
+        int grp_last = -1, n_last = -1;
+        float s_last = 0.0f;
+        auto load_scales = [&](int g, float (&dst)[4]) {
             if constexpr (KIND == KIND_W4A16) {
+                int m0, n0;
+                tile_of(g / p.nk, m0, n0);
+                const int n = n0 + row, kb = g % p.nk;
+                const int kc0 = kb * kBK + 8 * (4 * half), kc3 = kc0 + 24;
+                if (kc0 / p.G == kc3 / p.G) {
+                    const int grp = kc0 / p.G;
+                    if (grp != grp_last || n != n_last) {
+                        s_last = (n < p.N && kc0 < p.K)
+                                     ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + grp)))
+                                     : 0.0f;
+                        grp_last = grp;
+                        n_last = n;
+                    }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const int kcol = kb * kBK + 8 * (4 * half + c);
-                    dst[c] = (n < p.N && kcol < p.K)
-                                 ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + kcol / p.G)))
-                                 : 0.0f;
+                    for (int c = 0; c < 4; ++c) dst[c] = (kc0 + 8 * c < p.K) ? s_last : 0.0f;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int kcol = kc0 + 8 * c;
+                        dst[c] = (n < p.N && kcol < p.K)
+                                     ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + kcol / p.G)))
+                                     : 0.0f;
+                    }
+                    grp_last = -1;
                 }
             }
         };
-        load_scales(0, sc_cur);
-        bool ok = true;
-        for (int kb = 0; kb < p.nk; ++kb) {
-            const int s = kb % kStages;
-            if (kb + 1 < p.nk) load_scales(kb + 1, sc_nxt);
-            if (!wait_or_abort(&sh->tma_full[s], (kb / kStages) & 1, sh, p.status)) {
-                ok = false;
-                break;
-            }
+        if (total > 0) load_scales(0, sc_cur);
+        for (int g = 0; g < total; ++g) {
+            const int s = g % kStages;
+            if (g + 1 < total) load_scales(g + 1, sc_nxt);
+            if (!wait_or_abort(&sh->tma_full[s], (g / kStages) & 1, sh, p.status)) break;
             const uint8_t *prow = p_tiles + s * kPTile + row * kPRow;
             uint8_t *arow = a_row + s * kATile;
             if constexpr (KIND == KIND_W8A8) {
@@ -329,22 +375,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 #pragma unroll
             for (int c = 0; c < 4; ++c) sc_cur[c] = sc_nxt[c];
         }
-
-        // ---------------- epilogue: TMEM -> registers -> y
-        if (ok) ok = wait_or_abort(&sh->acc_full, 0, sh, p.status);
-        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
-        if (ok) {
+    } else {
+        // ---------------- epilogue (warps 2 + kConvWarps ..): TMEM -> registers -> y
+        const int q = warp & 3;                         // TMEM lane quadrant this warp may access
+        const int hc = (warp - 2 - kConvWarps) >> 2;    // column half
+        for (int i = 0; i < my_tiles; ++i) {
+            const int b = i & 1;
+            int m0, n0;
+            tile_of(i, m0, n0);
+            bool ok = wait_or_abort(&sh->acc_full[b], (i >> 1) & 1, sh, p.status);
+            ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+            if (!ok) break;
             tc_fence_after();
-            const int q = warp & 3;            // TMEM lane quadrant of this warp
-            const int hc = (warp - 2) >> 2;    // column half
             const int nrow = n0 + 32 * q + lane;
             float swn = 1.0f;
             if constexpr (KIND != KIND_W4A16) swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
-                const int col0 = 128 * hc + 32 * cc;
+            for (int cc = 0; cc < kBN / 64; ++cc) {
+                const int col0 = (kBN / 2) * hc + 32 * cc;
                 uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)col0, v);
+                tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(kBN * b + col0), v);
+                if (cc == kBN / 64 - 1) {
+                    // the accumulator is in registers: the MMA warp may reuse it
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sh->acc_empty[b]);
+                }
                 if (nrow < p.N) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -398,7 +454,11 @@ cudaError_t launch_kernel(const GemmParams &p, cudaStream_t st) {
         attr = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(KIND));
     });
     if (attr != cudaSuccess) return attr;
-    dim3 grid((unsigned)ceil_div(p.M, kBN), (unsigned)ceil_div(p.N, kBM));
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int grid = std::max(1, std::min(p.ntiles, sms));  // one persistent CTA per SM
     gemm_kernel<KIND><<<grid, kThreads, smem_bytes(KIND), st>>>(p);
     return cudaGetLastError();
 }
@@ -459,6 +519,8 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
         xsrc = a.workspace;
     }
     p.nk = (int)ceil_div(Kx, kBK);
+    p.ntn = (int)ceil_div(a.N, kBM);
+    p.ntiles = p.ntn * (int)ceil_div(a.M, kBN);
     {
         const uint64_t dims[2] = {(uint64_t)Kx, (uint64_t)a.M};
         const uint64_t strides[1] = {(uint64_t)Kx * 2};
