@@ -368,8 +368,11 @@ def time_steps(wl: Workload, steps: int, warmup: int, chunk: int = 256, kernel_o
     return e0.elapsed_time(e1), t0, t1
 
 
-def time_e2e(w, steps: int):
-    """Public API with host buffers: pinned x -> device, linear, y -> pinned host, every step."""
+def time_e2e(w, steps: int, chunk: int = 64):
+    """Public API with host buffers, every step: pinned x -> device, the
+    step's library calls, y -> pinned host.  The per-step sequence (copies
+    included) is captured once into a CUDA graph of `chunk` steps and
+    replayed, as a serving loop would run it."""
     import torch
     from w4a16_int4_quantized_gb300 import ops, synth
     M, N, K, G = w["M"], w["N"], w["K"], w["G"]
@@ -392,28 +395,54 @@ def time_e2e(w, steps: int):
         xh = torch.from_numpy(x).pin_memory()
         wq, sw = ops.quantize_matrix_q4(torch.from_numpy(W).cuda())
         xd = torch.empty_like(xh, device="cuda")
+        xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
         yd = torch.empty((M, N), dtype=torch.float32, device="cuda")
         yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        need = ops.workspace_bytes(ops.OP_LINEAR_Q4, M, N, K)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
 
         def step():
             xd.copy_(xh, non_blocking=True)
-            xq, sx, _ = ops.quantize_row_q8(xd)
-            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, out=yd)
+            st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
+            assert st == 0
+            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, out=yd, workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
-    for _ in range(5):
-        step()
+    stream = torch.cuda.Stream()
+    chunk = max(1, min(chunk, steps))
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(chunk):
+            step()
+    tail = None
+    if steps % chunk:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for _ in range(steps % chunk):
+                step()
+    with torch.cuda.stream(stream):
+        graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
-        step()
-    e1.record()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // chunk):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+        e1.record(stream)
     e1.synchronize()
     ms = e0.elapsed_time(e1)
     value, unit = metric_of(w, ms / steps)
     return {"value": value, "unit": unit, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(M * N * 4),
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms / steps,
+            "how": "per step: pinned host x -> device, the library calls, y -> pinned host; CUDA graph of "
+                   f"{chunk} steps replayed"}
 
 
 def prefill_lines(peaks):
