@@ -401,16 +401,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh->acc_empty[b]);
                 }
-                if (nrow < p.N) {
+                // sx of the chunk's 32 activation rows: one coalesced load, then shuffles
+                float sxl = 0.0f;
+                if constexpr (KIND != KIND_W4A16) sxl = (m0 + col0 + lane < p.M) ? p.sx[m0 + col0 + lane] : 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int m = m0 + col0 + j;
-                        if (m < p.M) {
-                            float out = __uint_as_float(v[j]);
-                            if constexpr (KIND != KIND_W4A16) out = __fmul_rn(__fmul_rn(out, p.sx[m]), swn);
-                            p.y[(size_t)m * p.N + nrow] = out;
-                        }
-                    }
+                for (int j = 0; j < 32; ++j) {  // every lane takes part in the shuffles
+                    const int m = m0 + col0 + j;
+                    float out = __uint_as_float(v[j]);
+                    if constexpr (KIND != KIND_W4A16)
+                        out = __fmul_rn(__fmul_rn(out, __shfl_sync(0xffffffffu, sxl, j)), swn);
+                    // streaming store: y is written once, the operand tiles stay in L2
+                    if (nrow < p.N && m < p.M) __stcs(p.y + (size_t)m * p.N + nrow, out);
                 }
             }
         }
