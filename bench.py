@@ -197,6 +197,26 @@ class ClockSampler:
         return out
 
 
+def max_over_ranks(ms: float, world: int) -> float:
+    """The slowest rank's time (replicas: every rank runs the whole workload;
+    the job takes as long as its slowest rank).  Works on either backend: a
+    CUDA tensor under NCCL, a CPU tensor under gloo."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], device=dev, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(per_rank_units: float, seconds: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas, each processing
+    `per_rank_units` in the slowest rank's `seconds`."""
+    return world * per_rank_units / seconds
+
+
 def dist_setup(n_gpus: int):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -820,17 +840,12 @@ def run_microdecoder(args, world, rank, local):
     time.sleep(0.2)
     sampler.stop()
     r = res["chain_rotating"]
-    ms = r["ms_per_frame"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(r["ms_per_frame"], world)
     status = ops.device_status()
     if rank != 0:
         return
     per_frame = wbytes * synth.MICRODECODER_PASSES
-    value = world * per_frame / (ms / 1e3) / 1e9
+    value = replica_value(per_frame, ms / 1e3, world) / 1e9
     e_ms, h2d, d2h = time_microdecoder_e2e(min(frames, 200))
     cpu = None
     if not args.no_cpu:
@@ -894,12 +909,9 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     time.sleep(0.2)
     sampler.stop()
-    ms_max = ms
+    ms_max = max_over_ranks(ms, world)
     if world > 1:
         import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
         dist.barrier()
     status = ops.device_status()
     value, unit = metric_of(w, ms_max / args.steps, world)
