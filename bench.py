@@ -72,6 +72,11 @@ WORKLOADS = {
     "w4a16_prefill_m2048_n3072": _wl("w4a16", 2048, 3072, 2048, 128, 0, "W4A16 prefill M=2048, K=2048, N=3072, G=128"),
     "w4a16_prefill_m2048_n13312": _wl("w4a16", 2048, 13312, 2048, 128, 0,
                                       "W4A16 prefill M=2048, K=2048, N=13312, G=128"),
+    "w4a16_prefill_m2048_n13312_il": _wl("w4a16", 2048, 13312, 2048, 128, 1,
+                                         "W4A16 prefill M=2048, K=2048, N=13312, G=128, straight from the "
+                                         "interleaved [N/64][K][32] layout"),
+    "w4a8_prefill_m2048_n13312_il": _wl("w4a8", 2048, 13312, 2048, 0, 1,
+                                        "W4A8 prefill M=2048, K=2048, N=13312, interleaved [N/64][K][32] layout"),
 }
 
 
@@ -486,6 +491,13 @@ def prefill_lines(peaks):
             "w4a8": lambda: ops.linear_q4(xq, sx, wq, sw, K=K, out=y, workspace=ws),
             "w4a16": lambda: ops.linear_w4a16_group(xbd, wbd, sbd, G, K=K, out=y),
         }
+        if N == 13312:
+            # prefill straight from the interleaved layout, same codes
+            wq_il, wb_il = ops.pack_interleaved_n64(wq, K), ops.pack_interleaved_n64(wbd, K)
+            runs["w4a8_il"] = lambda: ops.linear_q4(xq, sx, wq_il, sw, K=K, N=N, layout=ops.LAYOUT_N64, out=y,
+                                                    workspace=ws)
+            runs["w4a16_il"] = lambda: ops.linear_w4a16_group(xbd, wb_il, sbd, G, K=K, N=N, layout=ops.LAYOUT_N64,
+                                                              out=y)
         for name, fn in runs.items():
             for _ in range(3):
                 fn()
@@ -499,12 +511,14 @@ def prefill_lines(peaks):
             e1.synchronize()
             ms = e0.elapsed_time(e1) / reps
             tops = 2.0 * M * N * K / (ms / 1e3) / 1e12
-            out.append({"workload": f"{name}_prefill_m{M}_n{N}_k{K}", "metric": "TOPS" if name == "w4a8" else "TFLOP/s",
+            kind, _, lay = name.partition("_")
+            out.append({"workload": f"{kind}_prefill_m{M}_n{N}_k{K}" + (f"_{lay}" if lay else ""),
+                        "metric": "TOPS" if kind == "w4a8" else "TFLOP/s",
                         "value": round(tops, 1), "ms_per_call": round(ms, 4),
                         "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
                                      "frac": round(tops / bf16_peak, 4),
                                      "note": "f16/bf16 tcgen05 path; peak = measured bf16 dense sustained (f16 same rate)"}})
-            if name == "w4a8":
+            if kind == "w4a8":
                 out[-1]["roofline"]["int8_mma_sync_peak_tops"] = round(int8_peak, 1)
                 out[-1]["roofline"]["frac_of_int8_peak"] = round(tops / int8_peak, 3)
         del xq, wq, y, ws, xbd, wbd, sbd

@@ -124,15 +124,31 @@ def test_prefill_full_size_sampled(ops, ora, N):
     assert np.all(np.abs(yb[:, rows] - ye) <= 4e-3 * a + 1e-6)
 
 
-def test_gemm_interleaved_routes_correctly(ops, ora):
-    M, N, K, G = 40, 128, 512, 128
-    x, w, s = synth.w4a16_inputs(251, M, N, K, G)
+@pytest.mark.parametrize("M,N,K,G", [(40, 128, 512, 128), (300, 192, 1024, 32), (33, 2048, 2048, 128)])
+def test_gemm_interleaved_w4a16_matches_rowmajor(ops, ora, M, N, K, G):
+    """Prefill straight from the [N/64][K][32 B] layout: the same dequantised
+    bf16 tile as the row-major GEMM (the interleave is undone in shared
+    memory), so the same bits; N = 192 has an odd number of 64-channel blocks."""
+    x, w, s = synth.w4a16_inputs(251 + M + G, M, N, K, G)
     y = host(ops.linear_w4a16_group(dev(x), dev(w), dev(s), G, K=K))
     il = ops.pack_interleaved_n64(dev(w), K)
     y2 = host(ops.linear_w4a16_group(dev(x), il, dev(s), G, K=K, N=N, layout=ops.LAYOUT_N64))
+    assert np.array_equal(bits(y2), bits(y))
     ye, a = ora.linear_w4a16_exact(x, w, s, K, G)
-    assert np.all(np.abs(y2.astype(np.float64) - ye) <= 1e-5 * a + 1e-6)
-    assert np.all(np.abs(y.astype(np.float64) - ye) <= 4e-3 * a + 1e-6)
+    assert np.all(np.abs(y2.astype(np.float64) - ye) <= 4e-3 * a + 1e-6)
+
+
+@pytest.mark.parametrize("M,N,K", [(33, 128, 256), (300, 192, 1000), (64, 2048, 2047), (520, 384, 2048)])
+def test_gemm_interleaved_w4a8_bitexact(ops, ora, M, N, K):
+    """W4A8 prefill from the interleaved layout: bit-exact with the oracle
+    (ragged M, odd block count, K not a multiple of 64, odd K)."""
+    x, W = synth.w4a8_inputs(261 + M + N, M, N, K)
+    xq, sx, _ = ora.quantize_row_q8(x)
+    w, sw = ora.quantize_matrix_q4(W)
+    want = ora.linear_q4(xq, sx, w, sw, K)
+    il = ops.pack_interleaved_n64(dev(w), K)
+    y = host(ops.linear_q4(dev(xq), dev(sx), il, dev(sw), K=K, N=N, layout=ops.LAYOUT_N64))
+    assert np.array_equal(bits(y), bits(want))
 
 
 def test_gemm_device_status_clean(ops):

@@ -97,6 +97,14 @@ W4_DEV void tma_load_2d(void *dst, const void *map, int c0, int c1, uint64_t *ba
         : "memory");
 }
 
+// 3-D tiled TMA load of box (c0, c1, c2); c0 * element size must be a multiple of 16.
+W4_DEV void tma_load_3d(void *dst, const void *map, int c0, int c1, int c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // ---------------------------------------------------------------- PDL
 
 W4_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -153,6 +161,35 @@ W4_DEV uint4 lds_u128(uint32_t addr) {
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
     return v;
+}
+
+// 4x4 byte transpose + nibble repack of the interleaved layout: raw rows
+// [k][32 B] (byte d = channel d | channel d+32 << 4) of 8 consecutive k for
+// channels 4*dq..4*dq+3 -> one packed row-major word (8 nibbles, low first)
+// for each of the channels 4*dq+c (lo[c]) and 4*dq+c+32 (hi[c]).
+W4_DEV void deinterleave8(const uint8_t *raw, int dq, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint32_t *>(raw + i * 32 + 4 * dq);
+    uint32_t T[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t a01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x5140);
+        const uint32_t b01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x7362);
+        const uint32_t a23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x5140);
+        const uint32_t b23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x7362);
+        T[h][0] = prmt(a01, a23, 0x5410);  // byte i = column 4h+i of channel 4dq+0
+        T[h][1] = prmt(a01, a23, 0x7632);
+        T[h][2] = prmt(b01, b23, 0x5410);
+        T[h][3] = prmt(b01, b23, 0x7632);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t la = T[0][c] & 0x0F0F0F0Fu, lb = T[1][c] & 0x0F0F0F0Fu;
+        const uint32_t ha = (T[0][c] >> 4) & 0x0F0F0F0Fu, hb = (T[1][c] >> 4) & 0x0F0F0F0Fu;
+        lo[c] = prmt(la | (la >> 4), lb | (lb >> 4), 0x6420);
+        hi[c] = prmt(ha | (ha >> 4), hb | (hb >> 4), 0x6420);
+    }
 }
 
 W4_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -209,9 +209,14 @@ W4_DEV uint4 conv_w8a8(uint32_t lo, uint32_t hi) {
 
 // ---------------------------------------------------------------- kernel
 
-template <int KIND>
+// IL: the weights are in the interleaved [N/64][K][32 B] layout (vllm-omni
+// "The 4-bit CPU path"): the TMA brings two 64-channel blocks x 64 columns
+// per stage (the same 4 KB as the row-major tile) and the converters undo
+// the interleave with 4x4 byte transposes before the same dequantisation.
+template <int KIND, bool IL>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     constexpr bool kW4 = KIND != KIND_W8A8;
+    static_assert(!IL || kW4, "the interleaved layout holds int4 only");
     constexpr int kPRow = kW4 ? 32 : 64;             // packed bytes per weight row per stage
     constexpr int kATile = kBM * 128;                // 16 KB
     constexpr int kBTile = kBN * 128;                // 32 KB
@@ -265,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (g >= kStages && !wait_or_abort(&sh->empty[s], ((g / kStages) - 1) & 1, sh, p.status)) break;
                 mbar_arrive_expect_tx(&sh->tma_full[s], kStageTx);
                 tma_load_2d(b_tiles + s * kBTile, &p.xmap, kb * kBK, m0, &sh->tma_full[s]);
-                tma_load_2d(p_tiles + s * kPTile, &p.wmap, kb * kPRow, n0, &sh->tma_full[s]);
+                if constexpr (IL) tma_load_3d(p_tiles + s * kPTile, &p.wmap, 0, kb * kBK, n0 / 64, &sh->tma_full[s]);
+                else tma_load_2d(p_tiles + s * kPTile, &p.wmap, kb * kPRow, n0, &sh->tma_full[s]);
             }
         }
     } else if (warp == 1) {
@@ -297,8 +303,63 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (ok) umma_commit(&sh->acc_full[b]);
             }
         }
+    } else if (warp < 2 + kConvWarps && IL) {
+        // ---------------- weight conversion from the interleaved layout (256 threads)
+        // Thread: 64-channel block ib, 8-column group k8 of the stage, channel
+        // quad dq, low (channels 4dq+c) or high (4dq+c+32) half: four rows of A.
+        const int ct = tid - 64;
+        const int ib = ct >> 7, r = ct & 127, k8 = r >> 4, dq = (r >> 1) & 7, sel = r & 1;
+        // W4A16 scales of the four rows at this thread's columns, cached per
+        // (tile, group) and fetched one stage ahead (G % 32 == 0: one group per 8 columns)
+        float s_cur[4] = {0.f, 0.f, 0.f, 0.f}, s_nxt[4] = {0.f, 0.f, 0.f, 0.f};
+        int key_last = -1;
+        auto load_il_scales = [&](int g, float (&dst)[4]) {
+            if constexpr (KIND == KIND_W4A16) {
+                int m0, n0;
+                tile_of(g / p.nk, m0, n0);
+                const int col = (g % p.nk) * kBK + 8 * k8, grp = col / p.G;
+                const int key = (g / p.nk) * p.ng + grp;
+                if (key != key_last) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int n = n0 + 64 * ib + 4 * dq + c + 32 * sel;
+                        dst[c] = (n < p.N && col < p.K)
+                                     ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + grp)))
+                                     : 0.0f;
+                    }
+                    key_last = key;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) dst[c] = s_cur[c];
+                }
+            }
+        };
+        if (total > 0) {
+            key_last = -1;
+            load_il_scales(0, s_cur);
+        }
+        for (int g = 0; g < total; ++g) {
+            const int s = g % kStages;
+            if (g + 1 < total) load_il_scales(g + 1, s_nxt);
+            if (!wait_or_abort(&sh->tma_full[s], (g / kStages) & 1, sh, p.status)) break;
+            uint32_t lo[4], hi[4];
+            deinterleave8(p_tiles + s * kPTile + ib * 2048 + k8 * 8 * 32, dq, lo, hi);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int row = 64 * ib + 4 * dq + c + 32 * sel, rr = row & 7;
+                const uint32_t wd = sel ? hi[c] : lo[c];
+                uint4 v;
+                if constexpr (KIND == KIND_W4A16) v = conv_w4a16(wd, s_cur[c]);
+                else v = conv_w4a8(wd);
+                *reinterpret_cast<uint4 *>(a_tiles + s * kATile + (row >> 3) * 1024 + rr * 128 + ((k8 ^ rr) << 4)) = v;
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive(&sh->conv_full[s]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s_cur[c] = s_nxt[c];
+        }
     } else if (warp < 2 + kConvWarps) {
-        // ---------------- weight conversion (256 threads)
+        // ---------------- weight conversion, row-major layout (256 threads)
         const int ct = tid - 64;
         const int row = ct & (kBM - 1), half = ct >> 7;  // row of the tile, columns [32 half, 32 half + 32)
         const int rr = row & 7;
@@ -447,12 +508,13 @@ constexpr int smem_bytes(int kind) {
     return 1024 + kStages * (kBM * 128 + kBN * 128 + kBM * (kind == KIND_W8A8 ? 64 : 32)) + 1024;
 }
 
-template <int KIND>
+template <int KIND, bool IL>
 cudaError_t launch_kernel(const GemmParams &p, cudaStream_t st) {
     static std::once_flag once;
     static cudaError_t attr = cudaSuccess;
     std::call_once(once, [] {
-        attr = cudaFuncSetAttribute(gemm_kernel<KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes(KIND));
+        attr = cudaFuncSetAttribute(gemm_kernel<KIND, IL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    smem_bytes(KIND));
     });
     if (attr != cudaSuccess) return attr;
     int dev = 0, sms = 0;
@@ -460,7 +522,7 @@ cudaError_t launch_kernel(const GemmParams &p, cudaStream_t st) {
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const int grid = std::max(1, std::min(p.ntiles, sms));  // one persistent CTA per SM
-    gemm_kernel<KIND><<<grid, kThreads, smem_bytes(KIND), st>>>(p);
+    gemm_kernel<KIND, IL><<<grid, kThreads, smem_bytes(KIND), st>>>(p);
     return cudaGetLastError();
 }
 
@@ -470,11 +532,16 @@ int64_t kx_of(int64_t K) { return round_up(K, 8); }
 
 bool gemm_supported(const LinearArgs &a) {
     if (a.M <= 16) return false;
-    if (a.layout != W4_LAYOUT_ROWMAJOR) return false;
     if (a.N > 0x7FFFFFFF || a.M > 0x7FFFFFFF) return false;
     if (reinterpret_cast<uintptr_t>(a.w) % 16) return false;
-    const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
-    if (Kb % 16) return false;  // TMA row stride
+    if (a.layout == W4_LAYOUT_N64) {
+        // [N/64][K][32 B]: rows of 32 bytes, any K; W4A16 groups of whole 32-column chunks
+        if (a.kind == KIND_W8A8 || a.N % 64) return false;
+        if (a.kind == KIND_W4A16 && a.G % 32) return false;
+    } else {
+        const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
+        if (Kb % 16) return false;  // TMA row stride
+    }
     if (a.kind == KIND_W4A16) {
         if (a.K % 8 || a.G % 8) return false;  // bf16 rows for TMA; one scale per 8 columns
         if (reinterpret_cast<uintptr_t>(a.x) % 16) return false;
@@ -530,7 +597,16 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
                          2, xsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
-    {
+    const bool il = a.layout == W4_LAYOUT_N64;
+    if (il) {
+        // [N/64][K][32 B] as a 3-D tensor: box of 32 bytes x 64 columns x 2 blocks (128 channels)
+        const uint64_t dims[3] = {32, (uint64_t)a.K, (uint64_t)(a.N / 64)};
+        const uint64_t strides[2] = {32, (uint64_t)a.K * 32};
+        const uint32_t box[3] = {32, (uint32_t)kBK, (uint32_t)(kBM / 64)};
+        if (!encode_tmap(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, a.w, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
         const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
         const uint64_t dims[2] = {(uint64_t)Kb, (uint64_t)a.N};
         const uint64_t strides[1] = {(uint64_t)Kb};
@@ -540,9 +616,9 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
             return cudaErrorInvalidValue;
     }
     switch (a.kind) {
-        case KIND_W4A16: return launch_kernel<KIND_W4A16>(p, st);
-        case KIND_W4A8: return launch_kernel<KIND_W4A8>(p, st);
-        default: return launch_kernel<KIND_W8A8>(p, st);
+        case KIND_W4A16: return il ? launch_kernel<KIND_W4A16, true>(p, st) : launch_kernel<KIND_W4A16, false>(p, st);
+        case KIND_W4A8: return il ? launch_kernel<KIND_W4A8, true>(p, st) : launch_kernel<KIND_W4A8, false>(p, st);
+        default: return launch_kernel<KIND_W8A8, false>(p, st);
     }
 }
 

@@ -106,35 +106,6 @@ W4_DEV void unpack_signed_bf16(uint32_t w, uint32_t (&p)[4]) {
     }
 }
 
-// 4x4 byte transpose + nibble repack of the interleaved layout: raw rows
-// [k][32 B] (byte d = channel d | channel d+32 << 4) of 8 consecutive k for
-// channels 4*dq..4*dq+3 -> one packed row-major word (8 nibbles, low first)
-// for each of the channels 4*dq+c (lo[c]) and 4*dq+c+32 (hi[c]).
-W4_DEV void deinterleave8(const uint8_t *raw, int dq, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
-    uint32_t v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint32_t *>(raw + i * 32 + 4 * dq);
-    uint32_t T[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t a01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x5140);
-        const uint32_t b01 = prmt(v[4 * h + 0], v[4 * h + 1], 0x7362);
-        const uint32_t a23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x5140);
-        const uint32_t b23 = prmt(v[4 * h + 2], v[4 * h + 3], 0x7362);
-        T[h][0] = prmt(a01, a23, 0x5410);  // byte i = column 4h+i of channel 4dq+0
-        T[h][1] = prmt(a01, a23, 0x7632);
-        T[h][2] = prmt(b01, b23, 0x5410);
-        T[h][3] = prmt(b01, b23, 0x7632);
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t la = T[0][c] & 0x0F0F0F0Fu, lb = T[1][c] & 0x0F0F0F0Fu;
-        const uint32_t ha = (T[0][c] >> 4) & 0x0F0F0F0Fu, hb = (T[1][c] >> 4) & 0x0F0F0F0Fu;
-        lo[c] = prmt(la | (la >> 4), lb | (lb >> 4), 0x6420);
-        hi[c] = prmt(ha | (ha >> 4), hb | (hb >> 4), 0x6420);
-    }
-}
-
 // Biased nibbles (u = q + 8) of a word -> four f16x2 pairs of the exact
 // integers q: P0 = (k0, k4), P1 = (k1, k5), P2 = (k2, k6), P3 = (k3, k7).
 // 0x6400 | u is the f16 1024 + u; subtracting 1032 is exact.
