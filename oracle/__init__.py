@@ -97,6 +97,8 @@ class Oracle:
         L.ref_linear_w8a32.argtypes = [vp, vp, vp, vp, i64, i64, i64]
         L.ref_linear_w4a16_exact.restype = i32
         L.ref_linear_w4a16_exact.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64]
+        L.ref_linear_q4_group.restype = i32
+        L.ref_linear_q4_group.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64]
         L.ref_linear_w4a16_lanes.restype = i32
         L.ref_linear_w4a16_lanes.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64]
         L.ref_linear_w4a16_bf16dequant.restype = i32
@@ -223,6 +225,20 @@ class Oracle:
         y = np.zeros((M, N), np.float64)
         a = np.zeros((M, N), np.float64)
         rc = self.lib.ref_linear_w4a16_exact(_p(x), _p(w), _p(s), _p(y), _p(a), M, N, int(K), int(G))
+        assert rc == REF_OK, rc
+        return y, a
+
+    def linear_q4_group(self, xq, sx, w, s, z, K: int, G: int):
+        """Grouped asymmetric W4A8 in double: (y64, abs64)."""
+        xq = np.ascontiguousarray(xq, dtype=np.int8)
+        sx = np.ascontiguousarray(sx, dtype=np.float32)
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        s = np.ascontiguousarray(s, dtype=np.uint16)
+        z = np.ascontiguousarray(z, dtype=np.uint8)
+        M, N = xq.shape[0], w.shape[0]
+        y = np.zeros((M, N), np.float64)
+        a = np.zeros((M, N), np.float64)
+        rc = self.lib.ref_linear_q4_group(_p(xq), _p(sx), _p(w), _p(s), _p(z), _p(y), _p(a), M, N, int(K), int(G))
         assert rc == REF_OK, rc
         return y, a
 

@@ -33,6 +33,8 @@
  *   21 interleave pairs channels 2d and 2d+1 in byte d
  *   22 bias correction uses 7 instead of 8
  *   23 activation bf16 decoded as f16
+ *   24 grouped W4A8 zero point indexed by group only
+ *   25 grouped W4A8 zero points ignored (the constant 8 used)
  * (s11, the missing NULL check, would crash the test process and is covered
  * by the host-side validation tests of the CUDA library instead.)
  */
@@ -406,6 +408,58 @@ int ref_linear_w4a16_exact(const uint16_t *x, const uint8_t *w, const uint16_t *
             }
             y64[m * N + n] = acc;
             if (abs64) abs64[m * N + n] = aacc;
+        }
+    return REF_OK;
+}
+
+/* Grouped asymmetric W4A8 (vllm-omni "The 4-bit CPU path", "W4A8 --
+ * _C::int4_scaled_mm_cpu": GPTQ-style weights with the checkpoint's zero
+ * points, the constant 8 only when none are given; int8 activations):
+ *   acc_g   = sum over k in group g (k < K) of xq[m][k] * (u[n][k] - z[n][g])   (exact integer)
+ *   y64     = sx[m] * sum_g acc_g * s[n][g]                                      (double)
+ *   abs64   = sum over k of |xq[m][k] * sx[m] * (u[n][k] - z[n][g]) * s[n][g]|   (tolerance denominator)
+ * u are the raw stored nibbles (low nibble = even column), s f16 [N][Kp/G],
+ * z one byte per group [N][Kp/G].  Every product acc_g * s_g is exact in
+ * double; only the sum over groups rounds. */
+static int64_t zero_of(const uint8_t *z, int64_t n, int64_t ng, int64_t g) {
+#if MUT(24)
+    (void)n; (void)ng;
+    return z[g];
+#elif MUT(25)
+    (void)z; (void)n; (void)ng; (void)g;
+    return 8;
+#else
+    return z[n * ng + g];
+#endif
+}
+
+int ref_linear_q4_group(const int8_t *xq, const float *sx, const uint8_t *w, const uint16_t *s, const uint8_t *z,
+                        double *y64, double *abs64, int64_t M, int64_t N, int64_t K, int64_t G) {
+    const int rc = w4a16_check(xq, w, s, y64, M, N, K, G);
+    if (rc >= 0) return rc;
+    if (!sx || !z) return REF_EINVAL;
+    const int64_t Kb = (K + 1) / 2, Kp = K + (K & 1), ng = Kp / G;
+    const int64_t Nd = rows_done(N);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < Nd; ++n) {
+            const uint8_t *row = w + n * Kb;
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t g = 0; g < ng; ++g) {
+                const int64_t zz = zero_of(z, n, ng, g);
+                int64_t ig = 0, ia = 0;
+                for (int64_t i = 0; i < G; ++i) {
+                    const int64_t k = col_of(g, G, i);
+                    if (k >= K) continue;
+                    const int64_t p = (int64_t)xq[m * K + k] * ((int64_t)nib(row, k) - zz);
+                    ig += p;
+                    ia += p < 0 ? -p : p;
+                }
+                const double sg = scale_of(s, n, ng, g);
+                acc += (double)ig * sg;
+                aacc += (double)ia * fabs(sg);
+            }
+            y64[m * N + n] = (double)sx[m] * acc;
+            if (abs64) abs64[m * N + n] = fabs((double)sx[m]) * aacc;
         }
     return REF_OK;
 }

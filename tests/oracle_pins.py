@@ -345,6 +345,64 @@ def pin_shape_errors(o):
     assert st(0, 2, 4, 2) == REF_OK
 
 
+# ---------------------------------------------------------------- grouped asymmetric W4A8
+
+def np_dequant_q4_group(w, s, z, K: int, G: int) -> np.ndarray:
+    """W64[n, k] = (u[n, k] - z[n, k // G]) * f16(s[n, k // G]), raw nibbles decoded independently."""
+    u = np_unpack_codes(w, K, biased=True) + 8
+    g = np.arange(K) // G
+    return (u - np.asarray(z, np.int64)[:, g]).astype(np.float64) * np_f16(s)[:, g]
+
+
+def pin_q4_group_hand(o):
+    """Worked by hand (not printed on the pages): K = 4, G = 2, xq = [1, 2, 3, 4], sx = 1.
+    Row 0: u = [15, 8, 7, 12] (bytes 0x8F 0xC7), z = [8, 10], s = [0.5, 0.25]:
+      g0 = 1*7 + 2*0 = 7, g1 = 3*(-3) + 4*2 = -1, y = 7*0.5 - 0.25 = 3.25, sum|terms| = 3.5 + 17*0.25.
+    Row 1: u = [0, 15, 3, 3] (bytes 0xF0 0x33), z = [3, 3], s = [1, 2]:
+      g0 = 1*(-3) + 2*12 = 21, g1 = 0, y = 21."""
+    w = np.array([[0x8F, 0xC7], [0xF0, 0x33]], np.uint8)
+    s = np.array([[0x3800, 0x3400], [0x3C00, 0x4000]], np.uint16)
+    z = np.array([[8, 10], [3, 3]], np.uint8)
+    xq = np.array([[1, 2, 3, 4]], np.int8)
+    y, a = o.linear_q4_group(xq, np.ones(1, np.float32), w, s, z, 4, 2)
+    assert y[0, 0] == 3.25 and y[0, 1] == 21.0, y
+    assert a[0, 0] == 3.5 + 17 * 0.25 and a[0, 1] == 27.0, a
+
+
+def pin_q4_group_symmetric_is_linear_q4(o):
+    """Zero points all 8 and one scale per row: the grouped contract reduces to
+    the (pinned) per-channel linear_q4 -- up to linear_q4's two f32 roundings."""
+    M, N, K, G = 3, 29, 256, 64
+    x, W = synth.w4a8_inputs(700, M, N, K)
+    xq, sx, _ = o.quantize_row_q8(x)
+    w, sw = o.quantize_matrix_q4(W)
+    s16 = np.asarray(sw, np.float32).astype(np.float16)           # f16 scale, the same in every group
+    s = np.repeat(s16.view(np.uint16)[:, None], K // G, axis=1)
+    z = np.full((N, K // G), 8, np.uint8)
+    y, _ = o.linear_q4_group(xq, sx, w, s, z, K, G)
+    y1 = o.linear_q4(xq, sx, w, s16.astype(np.float32), K).astype(np.float64)
+    assert np.all(np.abs(y - y1) <= 2 * 2.0 ** -24 * np.abs(y1) + 1e-30)
+
+
+def pin_q4_group_random(o):
+    """Random codes, zero points and scales against a float64 matmul of the
+    independently dequantised weights; odd K; several groups per row."""
+    for (M, N, K, G) in ((2, 13, 96, 32), (3, 7, 255, 128), (1, 40, 1000, 8)):
+        Kp = K + (K & 1)
+        xq = synth.raw_bytes(710 + K, M * K).view(np.int8).reshape(M, K).copy()
+        xq[xq == -128] = -127
+        sx = (synth.uniform01(711 + K, M) + 0.5).astype(np.float32)
+        w = synth.raw_bytes(712 + K, N * (Kp // 2)).reshape(N, Kp // 2)
+        s = synth.group_scales_f16(713 + K, N, Kp // G)
+        z = (synth.raw_bytes(714 + K, N * (Kp // G)) & 0x0F).reshape(N, Kp // G)
+        y, a = o.linear_q4_group(xq, sx, w, s, z, K, G)
+        W64 = np_dequant_q4_group(w, s, z, K, G)
+        want = sx[:, None].astype(np.float64) * (xq.astype(np.float64) @ W64.T)
+        awant = np.abs(sx[:, None].astype(np.float64)) * (np.abs(xq.astype(np.float64)) @ np.abs(W64).T)
+        assert np.allclose(y, want, rtol=1e-12, atol=1e-9), (M, N, K, G)
+        assert np.allclose(a, awant, rtol=1e-12, atol=1e-9)
+
+
 PINS = {name[4:]: fn for name, fn in globals().items() if name.startswith("pin_")}
 
 
