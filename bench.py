@@ -77,6 +77,11 @@ WORKLOADS = {
                                          "interleaved [N/64][K][32] layout"),
     "w4a8_prefill_m2048_n13312_il": _wl("w4a8", 2048, 13312, 2048, 0, 1,
                                         "W4A8 prefill M=2048, K=2048, N=13312, interleaved [N/64][K][32] layout"),
+    "w4a8g_decode_m1_n13312": _wl("w4a8g", 1, 13312, 2048, 128, 0,
+                                  "grouped asymmetric W4A8 (f16 scales + zero points per group of 128), M=1, "
+                                  "K=2048, N=13312 (per-row Q8 quantize + linear)"),
+    "w4a8g_prefill_m2048_n13312": _wl("w4a8g", 2048, 13312, 2048, 128, 0,
+                                      "grouped asymmetric W4A8 prefill M=2048, K=2048, N=13312, G=128"),
 }
 
 
@@ -91,7 +96,12 @@ def weight_bytes(w) -> int:
     N, K, G = w["N"], w["K"], w["G"]
     kp = K + (K & 1)
     packed = N * (kp // 2)
-    scales = N * (kp // G) * 2 if w["kind"] == "w4a16" else N * 4
+    if w["kind"] == "w4a16":
+        scales = N * (kp // G) * 2
+    elif w["kind"] == "w4a8g":
+        scales = N * (kp // G) * 3  # f16 scale + one-byte zero point per group
+    else:
+        scales = N * 4
     return packed + scales
 
 
@@ -111,13 +121,14 @@ def metric_of(w, ms_per_step: float, n_gpus: int = 1):
     decode (M <= 16), tensor ops/s for prefill."""
     if w["regime"] == "decode":
         return n_gpus * weight_bytes(w) / (ms_per_step / 1e3) / 1e9, "GB/s"
-    return n_gpus * step_ops(w) / (ms_per_step / 1e3) / 1e12, ("TOPS" if w["kind"] == "w4a8" else "TFLOP/s")
+    return n_gpus * step_ops(w) / (ms_per_step / 1e3) / 1e12, ("TFLOP/s" if w["kind"] == "w4a16" else "TOPS")
 
 
 def metric_name(w) -> str:
     if w["regime"] == "decode":
         return f"int4 linear weight GB/s (M={w['M']} decode)"
-    return f"{'W4A8 TOPS' if w['kind'] == 'w4a8' else 'W4A16 TFLOP/s'} (M={w['M']} prefill)"
+    label = {"w4a8": "W4A8 TOPS", "w4a8g": "grouped W4A8 TOPS"}.get(w["kind"], "W4A16 TFLOP/s")
+    return f"{label} (M={w['M']} prefill)"
 
 
 # ---------------------------------------------------------------- helpers
@@ -256,6 +267,11 @@ def time_oracle(w, seconds: float, openmp: bool = True):
         x, wp, s = oracle_inputs(w)
         call = lambda: o.linear_w4a16_lanes(x, wp, s, w["K"], w["G"])
         what = "ref_linear_w4a16_lanes"
+    elif w["kind"] == "w4a8g":
+        from w4a16_int4_quantized_gb300 import synth
+        xq, sx, wp, s, z = synth.q4_group_inputs(1001, w["M"], w["N"], w["K"], w["G"])
+        call = lambda: o.linear_q4_group(xq, sx, wp, s, z, w["K"], w["G"])
+        what = "ref_linear_q4_group"
     else:
         x, W = oracle_inputs(w)
         xq, sx, _ = o.quantize_row_q8(x)
@@ -302,6 +318,21 @@ class Workload:
             self.wt = [w0.clone() for _ in range(copies)]
             self.s = [dev(s) for _ in range(copies)]
             self.ws = None
+        elif w["kind"] == "w4a8g":
+            _, _, wp, s, z = synth.q4_group_inputs(1001, 1, N, K, G)
+            xf = dev(synth.activations_f32(1001, M, K))
+            xq, sx, _ = ops.quantize_row_q8(xf)
+            w0 = dev(wp)
+            if w["layout"] == 1:
+                w0 = ops.pack_interleaved_n64(w0, K)
+            self.xf = [xf.clone() for _ in range(copies)]
+            self.x = [xq.clone() for _ in range(copies)]
+            self.sx = [sx.clone() for _ in range(copies)]
+            self.wt = [w0.clone() for _ in range(copies)]
+            self.s = [dev(s) for _ in range(copies)]
+            self.z = [dev(z) for _ in range(copies)]
+            need = ops.workspace_bytes(ops.OP_LINEAR_Q4_GROUP, M, N, K, G)
+            self.ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
         else:
             x, W = synth.w4a8_inputs(1001, M, N, K)
             xf = dev(x)
@@ -331,6 +362,9 @@ class Workload:
         if w["kind"] == "w4a16":
             ops.linear_w4a16_group(self.x[c], self.wt[c], self.s[c], w["G"], K=w["K"], N=w["N"],
                                    layout=w["layout"], flags=flags, out=self.y[c])
+        elif w["kind"] == "w4a8g":
+            ops.linear_q4_group(self.x[c], self.sx[c], self.wt[c], self.s[c], self.z[c], w["G"], K=w["K"],
+                                N=w["N"], layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
         else:
             ops.linear_q4(self.x[c], self.sx[c], self.wt[c], self.s[c], K=w["K"], N=w["N"],
                           layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
@@ -415,6 +449,25 @@ def time_e2e(w, steps: int, chunk: int = 64):
             ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, out=yd)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 2
+    elif w["kind"] == "w4a8g":
+        _, _, wp, s, z = synth.q4_group_inputs(1001, 1, N, K, G)
+        xh = torch.from_numpy(synth.activations_f32(1001, M, K)).pin_memory()
+        wd, sd, zd = torch.from_numpy(wp).cuda(), torch.from_numpy(s.view(np.int16)).cuda(), torch.from_numpy(z).cuda()
+        xd = torch.empty_like(xh, device="cuda")
+        xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
+        sx = torch.empty(M, dtype=torch.float32, device="cuda")
+        yd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        need = ops.workspace_bytes(ops.OP_LINEAR_Q4_GROUP, M, N, K, G)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+
+        def step():
+            xd.copy_(xh, non_blocking=True)
+            st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
+            assert st == 0
+            ops.linear_q4_group(xq, sx, wd, sd, zd, G, K=K, N=N, out=yd, workspace=ws)
+            yh.copy_(yd, non_blocking=True)
+        h2d = xh.numel() * 4
     else:
         x, W = synth.w4a8_inputs(1001, M, N, K)
         xh = torch.from_numpy(x).pin_memory()
@@ -976,7 +1029,8 @@ def run_ours(args, world, rank, local):
                    "G": w["G"], "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
                          f"({copies * weight_bytes(w) / 2**20:.0f} MiB of weights) vs L2 {l2 / 2**20:.0f} MiB",
-                   "step": "quantize_row_q8 + linear_q4" if w["kind"] == "w4a8" else "linear_w4a16_group",
+                   "step": {"w4a8": "quantize_row_q8 + linear_q4", "w4a8g": "quantize_row_q8 + linear_q4_group"}.get(
+                       w["kind"], "linear_w4a16_group"),
                    "timing": "CUDA events around CUDA-graph replays of exactly `steps` steps"},
         "roofline": roof,
         "cpu_baseline": cpu,

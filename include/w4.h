@@ -75,7 +75,7 @@ enum {
 };
 
 /* Operation ids for w4_workspace_bytes. */
-enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2 };
+enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2, W4_OP_LINEAR_Q4_GROUP = 3 };
 
 /* ---- quantizers ------------------------------------------------------------ */
 
@@ -187,6 +187,30 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
 #define W4_NOALLOC_SCRATCH_BYTES (8u << 20)
 w4_status w4_linear_q4_noalloc(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw, float *y,
                                int64_t M, int64_t N, int64_t K, int32_t layout, void *stream);
+
+/* ---- grouped asymmetric W4A8 ------------------------------------------------ */
+
+/* linear_q4_group: the GPTQ-style W4A8 of vllm-omni "The 4-bit CPU path"
+ * ("W4A8 -- _C::int4_scaled_mm_cpu": weights with per-group scales and the
+ * checkpoint's zero points, the constant 8 only when none are given; int8
+ * activations).  With u the stored nibble (low nibble = even column, the
+ * same packing as linear_q4):
+ *   acc[m][n][g] = sum_{k in group g} xq[m][k] * (u[n][k] - z[n][g])   exact in i32
+ *   y[m][n]      = sx[m] * sum_g acc * s[n][g]                        f32
+ * The sum over groups is in f32, order not fixed: |y - y_ref| <=
+ * 1e-5 * sum_k |xq * sx * (u - z) * s| + 1e-6 at M <= 16; the tensor-core
+ * path for M > 16 multiplies the f16 rounding of (u - z) * s (exact in f32)
+ * and is held to 4e-3 of the same sum.  Zero points all 8 with one scale per
+ * row give linear_q4 (to rounding).
+ * xq [M][K], sx [M] as for linear_q4; w packed [N][ceil(K/2)] (row-major) or
+ * [N/64][K][32] (W4_LAYOUT_N64); scales_f16 and zeros [N][Kp/G] (zero points
+ * 0..15, one byte each); y [M][N].
+ * workspace: w4_workspace_bytes(W4_OP_LINEAR_Q4_GROUP, M, N, K, G) bytes.
+ * ESHAPE: G <= 0, G odd or Kp % G != 0; layout N64 with N % 64 != 0.
+ * EINVAL: unknown layout; a NULL pointer. */
+w4_status w4_linear_q4_group(const int8_t *xq, const float *sx, const uint8_t *w, const uint16_t *scales_f16,
+                             const uint8_t *zeros, float *y, int64_t M, int64_t N, int64_t K, int64_t G,
+                             int32_t layout, void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
 
 /* ---- weight-resident chains -------------------------------------------------- */
 

@@ -140,3 +140,18 @@ def test_chain_validation(lib):
     assert need == 256 + 8 * (2 * 64 + 96)                              # header + pass output x2 + linear 0
     assert f(ok, wsb=need - 1) == lib.W4_EINVAL                          # workspace too small
     assert r.w4_chain_workspace_bytes(None, 2, 64) == 0
+
+
+def test_linear_q4_group_validation(lib):
+    r = lib.raw
+    f = lambda M, N, K, G, layout=0, z=FAKE: r.w4_linear_q4_group(FAKE, FAKE, FAKE, FAKE, z, FAKE, M, N, K, G,
+                                                                  layout, None, 0, 0, None)
+    assert f(-1, 2, 4, 2) == lib.W4_EINVAL
+    assert f(1, 2, 4, 2, layout=5) == lib.W4_EINVAL
+    assert f(1, 2, 4, 3) == lib.W4_ESHAPE          # G odd
+    assert f(1, 2, 12, 8) == lib.W4_ESHAPE         # Kp % G
+    assert f(1, 65, 4, 2, layout=1) == lib.W4_ESHAPE
+    assert f(0, 2, 4, 2) == lib.W4_OK
+    assert f(1, 2, 4, 2, z=None) == lib.W4_EINVAL  # zero points required
+    assert lib.workspace_bytes(lib.OP_LINEAR_Q4_GROUP, 1, 2048, 2048, 128) == 0
+    assert lib.workspace_bytes(lib.OP_LINEAR_Q4_GROUP, 2048, 2048, 2048, 128) > 0

@@ -190,6 +190,28 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
     return run_linear(a, as_stream(stream));
 }
 
+w4_status w4_linear_q4_group(const int8_t *xq, const float *sx, const uint8_t *w, const uint16_t *scales_f16,
+                             const uint8_t *zeros, float *y, int64_t M, int64_t N, int64_t K, int64_t G,
+                             int32_t layout, void *workspace, size_t ws_bytes, uint32_t flags, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64) return W4_EINVAL;
+    const int64_t Kp = K + (K & 1);
+    if (G <= 0 || (G & 1) || (Kp % G) != 0) return W4_ESHAPE;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (layout == W4_LAYOUT_N64 && N % 64) return W4_ESHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y || !sx || (K > 0 && (!xq || !w || !scales_f16 || !zeros))) return W4_EINVAL;
+    const w4_status ws = check_workspace(W4_OP_LINEAR_Q4_GROUP, M, N, K, G, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), as_stream(stream)));
+    w4::LinearArgs a = {};
+    a.kind = w4::KIND_W4A8G;
+    a.x = xq; a.w = w; a.scale = scales_f16; a.zeros = zeros; a.sx = sx; a.y = y;
+    a.M = M; a.N = N; a.K = K; a.G = G; a.layout = layout; a.flags = flags;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    return run_linear(a, as_stream(stream));
+}
+
 w4_status w4_pack_interleaved_n64(const uint8_t *w_rowmajor, uint8_t *w_il, int64_t N, int64_t K, void *stream) {
     if (N < 0 || K < 0) return W4_EINVAL;
     if (N % 64) return W4_ESHAPE;
@@ -244,6 +266,7 @@ size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G
         case W4_OP_LINEAR_Q4: return w4::gemm_workspace_bytes(w4::KIND_W4A8, M, N, K, G);
         case W4_OP_LINEAR_Q8: return w4::gemm_workspace_bytes(w4::KIND_W8A8, M, N, K, G);
         case W4_OP_LINEAR_W4A16: return w4::gemm_workspace_bytes(w4::KIND_W4A16, M, N, K, G);
+        case W4_OP_LINEAR_Q4_GROUP: return w4::gemm_workspace_bytes(w4::KIND_W4A8G, M, N, K, G);
         default: return 0;
     }
 }

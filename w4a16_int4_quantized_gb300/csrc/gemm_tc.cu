@@ -62,7 +62,8 @@ constexpr int kTmemCols = 512;  // two accumulators of kBN columns
 struct GemmParams {
     CUtensorMap xmap;  // 16-bit activations [M][Kx], box {64, 256}, 128B swizzle
     CUtensorMap wmap;  // packed weights [N][Kb] bytes, box {32|64, 128}
-    const uint16_t *scales;  // W4A16: f16 [N][ng]
+    const uint16_t *scales;  // W4A16, W4A8G: f16 [N][ng]
+    const uint8_t *zeros;    // W4A8G: zero points [N][ng]
     const float *sx;         // int kinds: [M]
     const float *sw;         // int kinds: [N]
     float *y;                // [M][N]
@@ -171,6 +172,22 @@ W4_DEV uint4 conv_w4a16(uint32_t w, float s) {
         const float qh = __int_as_float(0x4B000000 | (hi ^ 8u)) - 8388616.0f;
         __nv_bfloat162 b = __floats2bfloat162_rn(ql * s, qh * s);
         o[e] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// W4A8G: 8 packed nibbles (columns c..c+7) -> 8 f16 = f16_rne((u - z) * s):
+// (u - z) * s is exact in f32 and rounded once to f16.
+W4_DEV uint4 conv_w4a8g(uint32_t w, float s, float zb) {
+    // zb = 2^23 + z: (2^23 + u) - (2^23 + z) = u - z exactly
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t lo = (w >> (8 * e)) & 0xFu, hi = (w >> (8 * e + 4)) & 0xFu;
+        const float ql = __int_as_float(0x4B000000 | lo) - zb;
+        const float qh = __int_as_float(0x4B000000 | hi) - zb;
+        __half2 h = __floats2half2_rn(ql * s, qh * s);
+        o[e] = *reinterpret_cast<uint32_t *>(&h);
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
@@ -369,10 +386,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // consecutive stages share it when G > 64: each distinct scale is
         // loaded once (these row-strided loads cost a sector lookup per lane).
         float sc_cur[4] = {0.f, 0.f, 0.f, 0.f}, sc_nxt[4] = {0.f, 0.f, 0.f, 0.f};
+        float zb_cur = 8388608.0f, zb_nxt = 8388608.0f;  // W4A8G: 2^23 + zero point of the thread's group
         int grp_last = -1, n_last = -1;
-        float s_last = 0.0f;
+        float s_last = 0.0f, zb_last = 8388608.0f;
         auto load_scales = [&](int g, float (&dst)[4]) {
-            if constexpr (KIND == KIND_W4A16) {
+            if constexpr (KIND == KIND_W4A16 || KIND == KIND_W4A8G) {
                 int m0, n0;
                 tile_of(g / p.nk, m0, n0);
                 const int n = n0 + row, kb = g % p.nk;
@@ -380,12 +398,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (kc0 / p.G == kc3 / p.G) {
                     const int grp = kc0 / p.G;
                     if (grp != grp_last || n != n_last) {
-                        s_last = (n < p.N && kc0 < p.K)
-                                     ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + grp)))
-                                     : 0.0f;
+                        const bool in = n < p.N && kc0 < p.K;
+                        s_last = in ? __half2float(__ushort_as_half(__ldg(p.scales + (size_t)n * p.ng + grp))) : 0.0f;
+                        if constexpr (KIND == KIND_W4A8G)
+                            zb_last = 8388608.0f + (in ? (float)__ldg(p.zeros + (size_t)n * p.ng + grp) : 0.0f);
                         grp_last = grp;
                         n_last = n;
                     }
+                    zb_nxt = zb_last;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) dst[c] = (kc0 + 8 * c < p.K) ? s_last : 0.0f;
                 } else {
@@ -401,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             }
         };
         if (total > 0) load_scales(0, sc_cur);
+        zb_cur = zb_nxt;
         for (int g = 0; g < total; ++g) {
             const int s = g % kStages;
             if (g + 1 < total) load_scales(g + 1, sc_nxt);
@@ -425,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     uint4 v;
                     if constexpr (KIND == KIND_W4A16) {
                         v = conv_w4a16(wds[c], sc_cur[c]);
+                    } else if constexpr (KIND == KIND_W4A8G) {
+                        v = conv_w4a8g(wds[c], sc_cur[c], zb_cur);
                     } else {
                         v = conv_w4a8(wds[c]);
                     }
@@ -435,6 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             mbar_arrive(&sh->conv_full[s]);
 #pragma unroll
             for (int c = 0; c < 4; ++c) sc_cur[c] = sc_nxt[c];
+            zb_cur = zb_nxt;
         }
     } else {
         // ---------------- epilogue (warps 2 + kConvWarps ..): TMEM -> registers -> y
@@ -450,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             const int nrow = n0 + 32 * q + lane;
             float swn = 1.0f;
-            if constexpr (KIND != KIND_W4A16) swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
+            if constexpr (KIND == KIND_W4A8 || KIND == KIND_W8A8) swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
 #pragma unroll 1
             for (int cc = 0; cc < kBN / 64; ++cc) {
                 const int col0 = (kBN / 2) * hc + 32 * cc;
@@ -469,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 for (int j = 0; j < 32; ++j) {  // every lane takes part in the shuffles
                     const int m = m0 + col0 + j;
                     float out = __uint_as_float(v[j]);
-                    if constexpr (KIND != KIND_W4A16)
+                    if constexpr (KIND == KIND_W4A8G)
+                        out = __fmul_rn(out, __shfl_sync(0xffffffffu, sxl, j));  // sx * sum_g acc_g * s_g
+                    else if constexpr (KIND != KIND_W4A16)
                         out = __fmul_rn(__fmul_rn(out, __shfl_sync(0xffffffffu, sxl, j)), swn);
                     // streaming store: y is written once, the operand tiles stay in L2
                     if (nrow < p.N && m < p.M) __stcs(p.y + (size_t)m * p.N + nrow, out);
@@ -534,6 +560,7 @@ bool gemm_supported(const LinearArgs &a) {
     if (a.M <= 16) return false;
     if (a.N > 0x7FFFFFFF || a.M > 0x7FFFFFFF) return false;
     if (reinterpret_cast<uintptr_t>(a.w) % 16) return false;
+    if (a.kind == KIND_W4A8G && (a.layout != W4_LAYOUT_ROWMAJOR || a.G % 32)) return false;
     if (a.layout == W4_LAYOUT_N64) {
         // [N/64][K][32 B]: rows of 32 bytes, any K; W4A16 groups of whole 32-column chunks
         if (a.kind == KIND_W8A8 || a.N % 64) return false;
@@ -545,7 +572,7 @@ bool gemm_supported(const LinearArgs &a) {
     if (a.kind == KIND_W4A16) {
         if (a.K % 8 || a.G % 8) return false;  // bf16 rows for TMA; one scale per 8 columns
         if (reinterpret_cast<uintptr_t>(a.x) % 16) return false;
-    } else {
+    } else if (a.kind != KIND_W4A8G) {
         // exact integer accumulation in f32 needs 127 * max|q| * K < 2^24
         if (a.K > (a.kind == KIND_W4A8 ? 16384 : 1024)) return false;
     }
@@ -565,7 +592,8 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
     p.N = (int)a.N;
     p.K = (int)a.K;
     p.G = (int)a.G;
-    p.ng = (a.kind == KIND_W4A16) ? (int)((a.K + (a.K & 1)) / a.G) : 0;
+    p.ng = (a.kind == KIND_W4A16 || a.kind == KIND_W4A8G) ? (int)((a.K + (a.K & 1)) / a.G) : 0;
+    p.zeros = a.zeros;
     p.y = a.y;
     p.status = a.status;
     p.scales = static_cast<const uint16_t *>(a.scale);
@@ -618,6 +646,7 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
     switch (a.kind) {
         case KIND_W4A16: return il ? launch_kernel<KIND_W4A16, true>(p, st) : launch_kernel<KIND_W4A16, false>(p, st);
         case KIND_W4A8: return il ? launch_kernel<KIND_W4A8, true>(p, st) : launch_kernel<KIND_W4A8, false>(p, st);
+        case KIND_W4A8G: return launch_kernel<KIND_W4A8G, false>(p, st);
         default: return launch_kernel<KIND_W8A8, false>(p, st);
     }
 }

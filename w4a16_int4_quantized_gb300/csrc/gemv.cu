@@ -49,11 +49,16 @@
 namespace w4 {
 namespace {
 
+template <int KIND> constexpr bool kGrouped = KIND == KIND_W4A16 || KIND == KIND_W4A8G;  // f16 group scales
+template <int KIND> constexpr bool kIntAcc = KIND == KIND_W4A8 || KIND == KIND_W8A8;     // i32 accumulators
+template <int KIND> constexpr bool kBiased = KIND == KIND_W4A8 || KIND == KIND_W4A8G;    // u - 8 MMA operands
+
 struct GemvParams {
     const void *x;
     const uint8_t *w;
     const void *scale;
     const float *sx;
+    const uint8_t *zeros;  // W4A8G: [N][ng]
     float *y;
     uint32_t *status;
     int M, N, K;
@@ -70,6 +75,7 @@ struct GemvParams {
     int xstride;     // shared row stride of the activation tile (bytes)
     int sstride;     // shared row stride of the f32 scale tile (floats)
     int raw_off, w_off, x_off, sc_off, red_off;
+    int zc_off, xs_off;  // W4A8G: (8 - z) per [row][unit] (int), activation sums per [m][unit] (int)
     int x_vec;       // activation rows can be read with aligned vector loads
     int s_vec;       // scale rows can be read as 16-byte vectors
 };
@@ -188,7 +194,7 @@ W4_DEV void unit_mma(const uint8_t *w0, const uint8_t *w8, int c0, int g, int t,
             if constexpr (KIND == KIND_W4A16) {
                 unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w0 + wo), pa);
                 if (RB == 16) unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w8 + wo), pb);
-            } else if constexpr (KIND == KIND_W4A8) {
+            } else if constexpr (kBiased<KIND>) {
                 unpack_biased_f16(*reinterpret_cast<const uint32_t *>(w0 + wo), pa);
                 if (RB == 16) unpack_biased_f16(*reinterpret_cast<const uint32_t *>(w8 + wo), pb);
             } else {
@@ -227,9 +233,9 @@ W4_DEV bool prefetch_scales(const GemvParams &p, int row0, int rows, int u0, int
     const int tid = threadIdx.x;
     bool svec = false;
     const int spr = nun >> 3;  // 16-byte scale vectors per row
-    svec = (KIND == KIND_W4A16) && p.s_vec && rows * spr <= kMaxSc * nthr;
+    svec = kGrouped<KIND> && p.s_vec && rows * spr <= kMaxSc * nthr;
     const uint32_t spr_magic = div_magic((uint32_t)max(spr, 1));
-    if constexpr (KIND == KIND_W4A16) {
+    if constexpr (kGrouped<KIND>) {
         const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
         if (svec) {
 #pragma unroll
@@ -286,7 +292,7 @@ W4_DEV void stage_x(const GemvParams &p, int k0, int span_k, int nthr, uint8_t *
                 const uint32_t xsel4[4] = {0x0400u, 0x0501u, 0x0602u, 0x0703u};
                 const uint32_t xsel8[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
                 uint32_t b[4];
-                s8_to_f16_pairs(v.x, v.y, (KIND == KIND_W4A8) ? xsel4 : xsel8, b);
+                s8_to_f16_pairs(v.x, v.y, kBiased<KIND> ? xsel4 : xsel8, b);
                 o = make_uint4(b[0], b[1], b[2], b[3]);
             } else {
                 const uint16_t *xr = static_cast<const uint16_t *>(p.x) + (size_t)m * p.K;
@@ -316,7 +322,7 @@ W4_DEV void store_scales(const GemvParams &p, int rows, int nun, int nthr, bool 
     const int tid = threadIdx.x;
     const int spr = nun >> 3;
     const uint32_t spr_magic = div_magic((uint32_t)max(spr, 1));
-    if constexpr (KIND == KIND_W4A16) {
+    if constexpr (kGrouped<KIND>) {
         if (svec) {
             float *scf = reinterpret_cast<float *>(smem + p.sc_off);
 #pragma unroll
@@ -340,7 +346,7 @@ W4_DEV void store_scales(const GemvParams &p, int rows, int nun, int nthr, bool 
 template <int KIND, int RB, int MT, typename Acc>
 W4_DEV void combine_and_store(const GemvParams &p, Acc (&acc)[MT][4], int wr, int wk, int lane, int g, int t,
                               int rowbase, uint8_t *smem) {
-    constexpr bool kInt = KIND != KIND_W4A16;
+    constexpr bool kInt = kIntAcc<KIND>;
     // ---- 5. combine the K-split warps in index order.
     uint32_t *red = reinterpret_cast<uint32_t *>(smem + p.red_off);
     constexpr int kVals = MT * 4;
@@ -411,11 +417,50 @@ W4_DEV void combine_and_store(const GemvParams &p, Acc (&acc)[MT][4], int wr, in
             if constexpr (kInt) {
                 const float sw = static_cast<const float *>(p.scale)[n];
                 out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[mt][i]), p.sx[m]), sw);
+            } else if constexpr (KIND == KIND_W4A8G) {
+                out = __fmul_rn((float)acc[mt][i], p.sx[m]);  // sx * sum_g acc_g * s_g
             } else {
                 out = (float)acc[mt][i];
             }
             p.y[(size_t)m * p.N + n] = out;
         }
+}
+
+// W4A8G zero points of rows [row0, row0 + rows) x units [u0, u0 + nun) as
+// (8 - z) ints in shared memory (weights-side: loaded before the PDL wait).
+W4_DEV void load_zero_points(const GemvParams &p, int row0, int rows, int u0, int nun, int nthr, uint8_t *smem) {
+    int *zc = reinterpret_cast<int *>(smem + p.zc_off);
+    const uint32_t nun_magic = div_magic((uint32_t)nun);
+    for (int i = threadIdx.x; i < rows * nun; i += nthr) {
+        const int r = fast_div(i, nun_magic), gi = i - r * nun;
+        zc[r * p.sstride + gi] = 8 - (int)__ldg(p.zeros + (size_t)(row0 + r) * p.ng + u0 + gi);
+    }
+}
+
+// W4A8G: sum of the int8 activation codes of every (row m, unit) of the
+// CTA's span, for the zero-point correction (x-side: after the PDL wait).
+W4_DEV void stage_unit_sums(const GemvParams &p, int k0, int nun, int nthr, uint8_t *smem) {
+    int *xs = reinterpret_cast<int *>(smem + p.xs_off);
+    const uint32_t nun_magic = div_magic((uint32_t)nun);
+    const int8_t *x = static_cast<const int8_t *>(p.x);
+    for (int j = threadIdx.x; j < p.M * nun; j += nthr) {
+        const int m = fast_div(j, nun_magic), u = j - m * nun;
+        const int kb = k0 + u * p.unit_k, ke = min(p.K, kb + p.unit_k);
+        int sum = 0;
+        const int8_t *xr = x + (size_t)m * p.K;
+        int k = kb;
+        if (p.x_vec)
+            for (; k + 16 <= ke; k += 16) {
+                const int4 v = __ldg(reinterpret_cast<const int4 *>(xr + k));
+                const int one = 0x01010101;
+                sum = __dp4a(v.x, one, sum);
+                sum = __dp4a(v.y, one, sum);
+                sum = __dp4a(v.z, one, sum);
+                sum = __dp4a(v.w, one, sum);
+            }
+        for (; k < ke; ++k) sum += xr[k];
+        xs[m * p.upc + u] = sum;
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -480,10 +525,12 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     constexpr int kMaxSc = 2;
     uint4 sv[kMaxSc];
     const bool svec = prefetch_scales<KIND>(p, row0, rows, u0, nun, nthr, sv, smem);
+    if constexpr (KIND == KIND_W4A8G) load_zero_points(p, row0, rows, u0, nun, nthr, smem);
 
     griddep_wait();  // x may be written, and y read, by the previous kernel
 
     stage_x<KIND>(p, k0, span_k, nthr, smem);
+    if constexpr (KIND == KIND_W4A8G) stage_unit_sums(p, k0, nun, nthr, smem);
 
     // ---- 3. weight tile into shared memory (further rounds for big tiles).
     for (int base = 0; base < wchunks; base += kMaxLd * nthr) {
@@ -524,7 +571,7 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     griddep_launch_dependents();
 
     // ---- 4. tensor-core k-reduction.
-    using Acc = typename std::conditional<kInt, int, float>::type;
+    using Acc = typename std::conditional<kIntAcc<KIND>, int, float>::type;
     Acc acc[MT][4];
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
@@ -548,9 +595,28 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     const float *sc0 = scf + (rbase + g) * p.sstride;
     const float *sc1 = scf + (rbase + g + 8) * p.sstride;
 
+    const int *zc0 = reinterpret_cast<const int *>(smem + p.zc_off) + (rbase + g) * p.sstride;
+    const int *zc1 = reinterpret_cast<const int *>(smem + p.zc_off) + (rbase + g + 8) * p.sstride;
+    const int *xsum = reinterpret_cast<const int *>(smem + p.xs_off);
     // fold one unit's partial into acc (units arrive in increasing order)
     auto fold = [&](const float (&part)[MT][4], int u) {
-        if constexpr (KIND == KIND_W4A16) {
+        if constexpr (KIND == KIND_W4A8G) {
+            // exact group sum with the zero point: sum x*(u - 8) + (8 - z) * sum x, then * s_g
+            const float s0 = sc0[u];
+            const float s1 = (RB == 16) ? sc1[u] : 0.0f;
+            const int c0 = zc0[u];
+            const int c1 = (RB == 16) ? zc1[u] : 0;
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int ma = 8 * mt + 2 * t;
+                const int xa = ma < p.M ? xsum[ma * p.upc + u] : 0;
+                const int xb = ma + 1 < p.M ? xsum[(ma + 1) * p.upc + u] : 0;
+                acc[mt][0] = fmaf(s0, (float)(__float2int_rn(part[mt][0]) + c0 * xa), acc[mt][0]);
+                acc[mt][1] = fmaf(s0, (float)(__float2int_rn(part[mt][1]) + c0 * xb), acc[mt][1]);
+                acc[mt][2] = fmaf(s1, (float)(__float2int_rn(part[mt][2]) + c1 * xa), acc[mt][2]);
+                acc[mt][3] = fmaf(s1, (float)(__float2int_rn(part[mt][3]) + c1 * xb), acc[mt][3]);
+            }
+        } else if constexpr (KIND == KIND_W4A16) {
             const float s0 = sc0[u];
             const float s1 = (RB == 16) ? sc1[u] : 0.0f;
 #pragma unroll
@@ -775,7 +841,22 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
             const uint8_t b = p.w[((n >> 6) * p.K + k) * 32 + ((n & 63) & 31)];
             return ((n & 63) < 32) ? (b & 0xFu) : (b >> 4);
         };
-        if constexpr (KIND != KIND_W4A16) {
+        if constexpr (KIND == KIND_W4A8G) {
+            const int8_t *xr = static_cast<const int8_t *>(p.x) + m * p.K;
+            const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
+            const int64_t G = p.unit_k;
+            float out = 0.0f;
+            for (int64_t gi = 0; gi < p.ng; ++gi) {
+                const int z = p.zeros[n * p.ng + gi];
+                int acc = 0;
+                const int64_t kend = ((gi + 1) * G < p.K) ? (gi + 1) * G : (int64_t)p.K;
+                for (int64_t k = gi * G + lane; k < kend; k += 32) acc += (int)xr[k] * ((int)nibble(k) - z);
+#pragma unroll
+                for (int sft = 16; sft; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+                out = fmaf(__half2float(__ushort_as_half(s16[n * p.ng + gi])), (float)acc, out);
+            }
+            if (lane == 0) p.y[m * p.N + n] = __fmul_rn(out, p.sx[m]);
+        } else if constexpr (KIND != KIND_W4A16) {
             const int8_t *xr = static_cast<const int8_t *>(p.x) + m * p.K;
             int acc = 0;
             for (int64_t k = lane; k < p.K; k += 32) {
@@ -905,12 +986,12 @@ cudaError_t dispatch_rb_mt(const GemvParams &p, const Shape &s, int threads, int
     return launch_one<KIND, N64, 16, 2, CPG>(p, s.S, threads, smem, st, pdl);
 }
 
-template <bool N64>
-cudaError_t dispatch_w4a16(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
+template <int KIND, bool N64>
+cudaError_t dispatch_grouped(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
     switch (p.cpg) {
-        case 1: return dispatch_rb_mt<KIND_W4A16, N64, 1>(p, s, threads, smem, st, pdl);
-        case 4: return dispatch_rb_mt<KIND_W4A16, N64, 4>(p, s, threads, smem, st, pdl);
-        default: return dispatch_rb_mt<KIND_W4A16, N64, 0>(p, s, threads, smem, st, pdl);
+        case 1: return dispatch_rb_mt<KIND, N64, 1>(p, s, threads, smem, st, pdl);
+        case 4: return dispatch_rb_mt<KIND, N64, 4>(p, s, threads, smem, st, pdl);
+        default: return dispatch_rb_mt<KIND, N64, 0>(p, s, threads, smem, st, pdl);
     }
 }
 
@@ -927,7 +1008,7 @@ bool geometry(const LinearArgs &a, GemvParams &p) {
     } else if (a.kind == KIND_W4A8) {
         if (Kp % 32) return false;
         p.cpg = 1; p.unit_k = 32; p.unit_bytes = 16; p.units = (int)(Kp / 32); p.ng = 0;
-    } else {
+    } else {  // group-wise kinds: a unit is one group
         if (Kp % 32 || a.G % 32) return false;
         p.cpg = (int)(a.G / 32); p.unit_k = (int)a.G; p.unit_bytes = (int)(a.G / 2);
         p.units = (int)(Kp / a.G); p.ng = p.units;
@@ -956,7 +1037,15 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_ti
     p.x_off = off;
     off += (int)round_up((int64_t)a.M * p.xstride, 128);
     p.sc_off = off;
-    if (a.kind == KIND_W4A16) off += (int)round_up((int64_t)p.R * p.sstride * 4, 128);
+    const bool grouped = a.kind == KIND_W4A16 || a.kind == KIND_W4A8G;
+    if (grouped) off += (int)round_up((int64_t)p.R * p.sstride * 4, 128);
+    p.zc_off = off;
+    p.xs_off = off;
+    if (a.kind == KIND_W4A8G) {
+        off += (int)round_up((int64_t)p.R * p.sstride * 4, 128);
+        p.xs_off = off;
+        off += (int)round_up((int64_t)a.M * p.upc * 4, 128);
+    }
     p.red_off = off;
     const int warps = p.WR * p.WK;
     off += (int)round_up((int64_t)warps * 32 * ((a.M > 8) ? 8 : 4) * 4, 128);
@@ -982,6 +1071,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     p.w = a.w;
     p.scale = a.scale;
     p.sx = a.sx;
+    p.zeros = a.zeros;
     p.y = a.y;
     p.status = a.status;
     p.M = (int)a.M;
@@ -1038,7 +1128,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     if (smem > kSmemLimit) return launch_generic(a, st);
 
     p.x_vec = ((a.K * esize) % 16 == 0 && reinterpret_cast<uintptr_t>(a.x) % 16 == 0) ? 1 : 0;
-    p.s_vec = (a.kind == KIND_W4A16 && p.ng % 8 == 0 && p.upc % 8 == 0 &&
+    p.s_vec = ((a.kind == KIND_W4A16 || a.kind == KIND_W4A8G) && p.ng % 8 == 0 && p.upc % 8 == 0 &&
                reinterpret_cast<uintptr_t>(a.scale) % 16 == 0) ? 1 : 0;
     s.S = S;
     const int threads = 32 * p.WR * p.WK;
@@ -1047,7 +1137,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     // from global memory, so shared memory holds only x and the scales and
     // more CTAs fit per SM (the same arithmetic, so the same bits).  For
     // M <= 8 the 128-bit staged tile streams HBM better.
-    if (!n64 && a.M > 8 && a.kind != KIND_W8A8 && (p.cpg == 1 || p.cpg == 2 || p.cpg == 4) &&
+    if (!n64 && a.M > 8 && (a.kind == KIND_W4A16 || a.kind == KIND_W4A8) && (p.cpg == 1 || p.cpg == 2 || p.cpg == 4) &&
         (a.kind == KIND_W4A16 || p.cpg == 1)) {
         GemvParams q = p;
         const int dsmem = plan_smem(a, s, q, false);
@@ -1064,9 +1154,12 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
                        : dispatch_rb_mt<KIND_W4A8, false, 1>(p, s, threads, smem, st, pdl);
         case KIND_W8A8:
             return dispatch_rb_mt<KIND_W8A8, false, 1>(p, s, threads, smem, st, pdl);
+        case KIND_W4A8G:
+            return n64 ? dispatch_grouped<KIND_W4A8G, true>(p, s, threads, smem, st, pdl)
+                       : dispatch_grouped<KIND_W4A8G, false>(p, s, threads, smem, st, pdl);
         default:
-            return n64 ? dispatch_w4a16<true>(p, s, threads, smem, st, pdl)
-                       : dispatch_w4a16<false>(p, s, threads, smem, st, pdl);
+            return n64 ? dispatch_grouped<KIND_W4A16, true>(p, s, threads, smem, st, pdl)
+                       : dispatch_grouped<KIND_W4A16, false>(p, s, threads, smem, st, pdl);
     }
 }
 
@@ -1076,12 +1169,13 @@ cudaError_t launch_generic(const LinearArgs &a, cudaStream_t st) {
     p.w = a.w;
     p.scale = a.scale;
     p.sx = a.sx;
+    p.zeros = a.zeros;
     p.y = a.y;
     p.status = a.status;
     p.M = (int)a.M;
     p.N = (int)a.N;
     p.K = (int)a.K;
-    if (a.kind == KIND_W4A16) {
+    if (a.kind == KIND_W4A16 || a.kind == KIND_W4A8G) {
         const int64_t Kp = a.K + (a.K & 1);
         p.ng = (int)(Kp / a.G);
         p.unit_k = (int)a.G;
@@ -1091,6 +1185,7 @@ cudaError_t launch_generic(const LinearArgs &a, cudaStream_t st) {
     switch (a.kind) {
         case KIND_W4A8: generic_kernel<KIND_W4A8><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
         case KIND_W8A8: generic_kernel<KIND_W8A8><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
+        case KIND_W4A8G: generic_kernel<KIND_W4A8G><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
         default: generic_kernel<KIND_W4A16><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
     }
     return cudaGetLastError();

@@ -10,7 +10,8 @@
 
 namespace w4 {
 
-enum Kind : int { KIND_W4A8 = 0, KIND_W8A8 = 1, KIND_W4A16 = 2 };
+// W4A8G: grouped asymmetric W4A8 (per-group f16 scales and zero points).
+enum Kind : int { KIND_W4A8 = 0, KIND_W8A8 = 1, KIND_W4A16 = 2, KIND_W4A8G = 3 };
 
 // One linear call after host validation (shapes legal, pointers non-NULL,
 // M, N, K > 0).
@@ -18,7 +19,8 @@ struct LinearArgs {
     int kind;
     const void *x;       // int8 [M][K] (W4A8, W8A8) or bf16 [M][K] (W4A16)
     const uint8_t *w;    // packed int4 (layout) or int8 [N][K]
-    const void *scale;   // f32 sw [N] (int kinds) or f16 [N][Kp/G] (W4A16)
+    const void *scale;   // f32 sw [N] (W4A8, W8A8) or f16 [N][Kp/G] (W4A16, W4A8G)
+    const uint8_t *zeros;  // W4A8G: zero points [N][Kp/G]
     const float *sx;     // f32 [M] (int kinds)
     float *y;            // f32 [M][N]
     int64_t M, N, K, G;  // G: W4A16 only

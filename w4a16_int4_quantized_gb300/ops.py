@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libw4gb300.so")
 W4_OK, W4_EINVAL, W4_ESHAPE, W4_ECUDA = 0, 1, 2, 3
 LAYOUT_ROWMAJOR, LAYOUT_N64 = 0, 1
 FLAG_PDL = 1
-OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16 = 0, 1, 2
+OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16, OP_LINEAR_Q4_GROUP = 0, 1, 2, 3
 CHAIN_MAX_LINEARS, CHAIN_MAX_K = 64, 8192
 
 
@@ -43,6 +43,7 @@ SIGNATURES = [
     ("w4_linear_q8", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_noalloc", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    ("w4_linear_q4_group", _i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_chain_q4", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
     ("w4_chain_workspace_bytes", _sz, [_vp, _i32, _i32]),
     ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
@@ -210,6 +211,20 @@ def linear_w4a16_group(x, w, scales, G: int, K: int | None = None, N: int | None
     ws, wsb = _workspace(OP_LINEAR_W4A16, M, N, K, G, workspace, x.device)
     _check(raw.w4_linear_w4a16_group(_ptr(x), _ptr(w), _ptr(scales), _ptr(y), M, N, K, G, layout,
                                      _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_w4a16_group")
+    return y
+
+
+def linear_q4_group(xq, sx, w, scales, zeros, G: int, K: int | None = None, N: int | None = None,
+                    layout: int = LAYOUT_ROWMAJOR, flags: int = 0, out=None, workspace=None,
+                    stream=None) -> torch.Tensor:
+    """Grouped asymmetric W4A8: y = sx[m] * sum_g (sum_{k in g} xq * (u - z[n, g])) * s[n, g]."""
+    M = xq.shape[0]
+    K = xq.shape[1] if K is None else K
+    N = scales.shape[0] if N is None else N
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=xq.device)
+    ws, wsb = _workspace(OP_LINEAR_Q4_GROUP, M, N, K, G, workspace, xq.device)
+    _check(raw.w4_linear_q4_group(_ptr(xq), _ptr(sx), _ptr(w), _ptr(scales), _ptr(zeros), _ptr(y), M, N, K, G,
+                                  layout, _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_q4_group")
     return y
 
 

@@ -129,6 +129,20 @@ def w4a8_inputs(seed: int, m: int, n: int, k: int):
     return activations_f32(seed, m, k), weights_f32(seed + 1, n, k)
 
 
+def q4_group_inputs(seed: int, m: int, n: int, k: int, g: int):
+    """Grouped asymmetric W4A8 inputs: int8 codes xq [m, k] in [-127, 127],
+    sx [m] in [0.5, 1.5), raw nibbles (every value 0..15) packed [n, kp/2],
+    f16 scales and zero points 0..15, both [n, kp/g]."""
+    kp = k + (k & 1)
+    xq = raw_bytes(seed, m * k).view(np.int8).reshape(m, k).copy()
+    xq[xq == -128] = -127
+    sx = (uniform01(seed + 1, m) + 0.5).astype(np.float32)
+    w = raw_bytes(seed + 2, n * (kp // 2)).reshape(n, kp // 2)
+    s = group_scales_f16(seed + 3, n, kp // g)
+    z = (raw_bytes(seed + 4, n * (kp // g)) & 0x0F).reshape(n, kp // g)
+    return xq, sx, w, s, z
+
+
 MICRODECODER_LAYERS = 5
 MICRODECODER_PASSES = 15
 # (name, N, K) of one microdecoder layer, in dataflow order.
