@@ -77,6 +77,11 @@ WORKLOADS = {
                                          "interleaved [N/64][K][32] layout"),
     "w4a8_prefill_m2048_n13312_il": _wl("w4a8", 2048, 13312, 2048, 0, 1,
                                         "W4A8 prefill M=2048, K=2048, N=13312, interleaved [N/64][K][32] layout"),
+    "w8a16_decode_m1_n13312": _wl("w8a16", 1, 13312, 2048, 0, 0,
+                                  "linear_w8a16 (int8 weights, f32 channel scales, f32 activations), M=1, K=2048, "
+                                  "N=13312"),
+    "w8a16_prefill_m2048_n13312": _wl("w8a16", 2048, 13312, 2048, 0, 0,
+                                      "linear_w8a16 prefill M=2048, K=2048, N=13312"),
     "w4a8g_decode_m1_n13312": _wl("w4a8g", 1, 13312, 2048, 128, 0,
                                   "grouped asymmetric W4A8 (f16 scales + zero points per group of 128), M=1, "
                                   "K=2048, N=13312 (per-row Q8 quantize + linear)"),
@@ -95,7 +100,7 @@ TRAFFIC = {
 def weight_bytes(w) -> int:
     N, K, G = w["N"], w["K"], w["G"]
     kp = K + (K & 1)
-    packed = N * (kp // 2)
+    packed = N * K if w["kind"] == "w8a16" else N * (kp // 2)
     if w["kind"] == "w4a16":
         scales = N * (kp // G) * 2
     elif w["kind"] == "w4a8g":
@@ -108,7 +113,7 @@ def weight_bytes(w) -> int:
 def step_bytes(w) -> int:
     """Algorithmic bytes of one linear launch: weights + scales + activations + output."""
     M, N, K = w["M"], w["N"], w["K"]
-    xb = M * K * (2 if w["kind"] == "w4a16" else 1) + (0 if w["kind"] == "w4a16" else 4 * M)
+    xb = {"w4a16": M * K * 2, "w8a16": M * K * 4}.get(w["kind"], M * K + 4 * M)
     return weight_bytes(w) + xb + M * N * 4
 
 
@@ -121,13 +126,15 @@ def metric_of(w, ms_per_step: float, n_gpus: int = 1):
     decode (M <= 16), tensor ops/s for prefill."""
     if w["regime"] == "decode":
         return n_gpus * weight_bytes(w) / (ms_per_step / 1e3) / 1e9, "GB/s"
-    return n_gpus * step_ops(w) / (ms_per_step / 1e3) / 1e12, ("TFLOP/s" if w["kind"] == "w4a16" else "TOPS")
+    return n_gpus * step_ops(w) / (ms_per_step / 1e3) / 1e12, ("TFLOP/s" if w["kind"] in ("w4a16", "w8a16")
+                                                               else "TOPS")
 
 
 def metric_name(w) -> str:
     if w["regime"] == "decode":
-        return f"int4 linear weight GB/s (M={w['M']} decode)"
-    label = {"w4a8": "W4A8 TOPS", "w4a8g": "grouped W4A8 TOPS"}.get(w["kind"], "W4A16 TFLOP/s")
+        return f"{'int8' if w['kind'] == 'w8a16' else 'int4'} linear weight GB/s (M={w['M']} decode)"
+    label = {"w4a8": "W4A8 TOPS", "w4a8g": "grouped W4A8 TOPS", "w8a16": "W8A16 TFLOP/s"}.get(w["kind"],
+                                                                                             "W4A16 TFLOP/s")
     return f"{label} (M={w['M']} prefill)"
 
 
@@ -267,6 +274,13 @@ def time_oracle(w, seconds: float, openmp: bool = True):
         x, wp, s = oracle_inputs(w)
         call = lambda: o.linear_w4a16_lanes(x, wp, s, w["K"], w["G"])
         what = "ref_linear_w4a16_lanes"
+    elif w["kind"] == "w8a16":
+        from w4a16_int4_quantized_gb300 import synth
+        x = synth.activations_f32(1001, w["M"], w["K"])
+        wq = synth.raw_bytes(1002, w["N"] * w["K"]).view(np.int8).reshape(w["N"], w["K"])
+        sw = np.full(w["N"], 1e-3, np.float32)
+        call = lambda: o.linear_w8a16_exact(x, wq, sw)
+        what = "ref_linear_w8a16_exact"
     elif w["kind"] == "w4a8g":
         from w4a16_int4_quantized_gb300 import synth
         xq, sx, wp, s, z = synth.q4_group_inputs(1001, w["M"], w["N"], w["K"], w["G"])
@@ -318,6 +332,14 @@ class Workload:
             self.wt = [w0.clone() for _ in range(copies)]
             self.s = [dev(s) for _ in range(copies)]
             self.ws = None
+        elif w["kind"] == "w8a16":
+            x0 = dev(synth.activations_f32(1001, M, K))
+            w0 = dev(synth.raw_bytes(1002, N * K).view(np.int8).reshape(N, K))
+            self.x = [x0.clone() for _ in range(copies)]
+            self.wt = [w0.clone() for _ in range(copies)]
+            self.s = [torch.full((N,), 1e-3, dtype=torch.float32, device="cuda") for _ in range(copies)]
+            need = ops.workspace_bytes(ops.OP_LINEAR_W8A16, M, N, K)
+            self.ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
         elif w["kind"] == "w4a8g":
             _, _, wp, s, z = synth.q4_group_inputs(1001, 1, N, K, G)
             xf = dev(synth.activations_f32(1001, M, K))
@@ -354,6 +376,8 @@ class Workload:
     def launches_per_step(self) -> int:
         if self.w["kind"] == "w4a16":
             return 1
+        if self.w["kind"] == "w8a16":
+            return 1 + (1 if self.ws is not None else 0)  # (f32 -> bf16 prepass), linear
         return 2 + (1 if self.ws is not None else 0)  # quantize, (int8 -> f16 prepass), linear
 
     def kernel(self, i: int, flags: int = 1):
@@ -362,6 +386,8 @@ class Workload:
         if w["kind"] == "w4a16":
             ops.linear_w4a16_group(self.x[c], self.wt[c], self.s[c], w["G"], K=w["K"], N=w["N"],
                                    layout=w["layout"], flags=flags, out=self.y[c])
+        elif w["kind"] == "w8a16":
+            ops.linear_w8a16(self.x[c], self.wt[c], self.s[c], flags=flags, out=self.y[c], workspace=self.ws)
         elif w["kind"] == "w4a8g":
             ops.linear_q4_group(self.x[c], self.sx[c], self.wt[c], self.s[c], self.z[c], w["G"], K=w["K"],
                                 N=w["N"], layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
@@ -370,7 +396,7 @@ class Workload:
                           layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
 
     def step(self, i: int, flags: int = 1):
-        if self.w["kind"] != "w4a16":
+        if self.w["kind"] not in ("w4a16", "w8a16"):
             c = i % self.copies
             M, K = self.xf[c].shape
             st = self.ops.raw.w4_quantize_row_q8(self.xf[c].data_ptr(), M, K, self.x[c].data_ptr(),
@@ -449,6 +475,21 @@ def time_e2e(w, steps: int, chunk: int = 64):
             ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, out=yd)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 2
+    elif w["kind"] == "w8a16":
+        xh = torch.from_numpy(synth.activations_f32(1001, M, K)).pin_memory()
+        wd = torch.from_numpy(synth.raw_bytes(1002, N * K).view(np.int8).reshape(N, K).copy()).cuda()
+        sd = torch.full((N,), 1e-3, dtype=torch.float32, device="cuda")
+        xd = torch.empty_like(xh, device="cuda")
+        yd = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        need = ops.workspace_bytes(ops.OP_LINEAR_W8A16, M, N, K)
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+
+        def step():
+            xd.copy_(xh, non_blocking=True)
+            ops.linear_w8a16(xd, wd, sd, out=yd, workspace=ws)
+            yh.copy_(yd, non_blocking=True)
+        h2d = xh.numel() * 4
     elif w["kind"] == "w4a8g":
         _, _, wp, s, z = synth.q4_group_inputs(1001, 1, N, K, G)
         xh = torch.from_numpy(synth.activations_f32(1001, M, K)).pin_memory()
@@ -1024,12 +1065,13 @@ def run_ours(args, world, rank, local):
         "metric": metric_name(w),
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w["kind"] == "w4a16" else "s8", "data": "synthetic",
+        "dtype": {"w4a16": "bf16", "w8a16": "f32"}.get(w["kind"], "s8"), "data": "synthetic",
         "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"], "N": w["N"], "K": w["K"],
                    "G": w["G"], "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
                          f"({copies * weight_bytes(w) / 2**20:.0f} MiB of weights) vs L2 {l2 / 2**20:.0f} MiB",
-                   "step": {"w4a8": "quantize_row_q8 + linear_q4", "w4a8g": "quantize_row_q8 + linear_q4_group"}.get(
+                   "step": {"w4a8": "quantize_row_q8 + linear_q4", "w4a8g": "quantize_row_q8 + linear_q4_group",
+                            "w8a16": "linear_w8a16"}.get(
                        w["kind"], "linear_w4a16_group"),
                    "timing": "CUDA events around CUDA-graph replays of exactly `steps` steps"},
         "roofline": roof,

@@ -75,7 +75,8 @@ enum {
 };
 
 /* Operation ids for w4_workspace_bytes. */
-enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2, W4_OP_LINEAR_Q4_GROUP = 3 };
+enum { W4_OP_LINEAR_Q4 = 0, W4_OP_LINEAR_Q8 = 1, W4_OP_LINEAR_W4A16 = 2, W4_OP_LINEAR_Q4_GROUP = 3,
+       W4_OP_LINEAR_W8A16 = 4 };
 
 /* ---- quantizers ------------------------------------------------------------ */
 
@@ -187,6 +188,19 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
 #define W4_NOALLOC_SCRATCH_BYTES (8u << 20)
 w4_status w4_linear_q4_noalloc(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw, float *y,
                                int64_t M, int64_t N, int64_t K, int32_t layout, void *stream);
+
+/* linear_w8a16 (docs.rs ftts_kernels::int8, linear_w8a16): f32 activations
+ * times the per-channel Q8 matrix of w4_quantize_matrix_q8:
+ *   y[m][n] = sw[n] * sum_k x[m][k] * q[n][k]   (f32, summation order not fixed)
+ * |y - y_ref| <= 1e-5 * sum_k |x * q * sw| + 1e-6 for M <= 16 (x enters the
+ * tensor cores as two bf16 terms, hi = bf16(x) and lo = bf16(x - hi), within
+ * 2^-18 of x; the products with the int8 codes are exact); the tensor-core
+ * path for M > 16 rounds x to bf16 once and is held to 4e-3.
+ * x f32 [M][K]; w int8 [N][K]; sw [N]; y [M][N].
+ * workspace: w4_workspace_bytes(W4_OP_LINEAR_W8A16, M, N, K, 0) bytes (the
+ * bf16 image of x when M > 16).  EINVAL: a NULL pointer. */
+w4_status w4_linear_w8a16(const float *x, const int8_t *w, const float *sw, float *y, int64_t M, int64_t N,
+                          int64_t K, void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
 
 /* ---- grouped asymmetric W4A8 ------------------------------------------------ */
 

@@ -97,6 +97,8 @@ class Oracle:
         L.ref_linear_w8a32.argtypes = [vp, vp, vp, vp, i64, i64, i64]
         L.ref_linear_w4a16_exact.restype = i32
         L.ref_linear_w4a16_exact.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64]
+        L.ref_linear_w8a16_exact.restype = i32
+        L.ref_linear_w8a16_exact.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64]
         L.ref_linear_q4_group.restype = i32
         L.ref_linear_q4_group.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64]
         L.ref_linear_w4a16_lanes.restype = i32
@@ -225,6 +227,19 @@ class Oracle:
         y = np.zeros((M, N), np.float64)
         a = np.zeros((M, N), np.float64)
         rc = self.lib.ref_linear_w4a16_exact(_p(x), _p(w), _p(s), _p(y), _p(a), M, N, int(K), int(G))
+        assert rc == REF_OK, rc
+        return y, a
+
+    def linear_w8a16_exact(self, x, wq, sw):
+        """linear_w8a16 in double: (y64, abs64)."""
+        x = np.ascontiguousarray(x, dtype=np.float32)
+        wq = np.ascontiguousarray(wq, dtype=np.int8)
+        sw = np.ascontiguousarray(sw, dtype=np.float32)
+        M, K = x.shape
+        N = wq.shape[0]
+        y = np.zeros((M, N), np.float64)
+        a = np.zeros((M, N), np.float64)
+        rc = self.lib.ref_linear_w8a16_exact(_p(x), _p(wq), _p(sw), _p(y), _p(a), M, N, K)
         assert rc == REF_OK, rc
         return y, a
 

@@ -319,6 +319,37 @@ int ref_linear_q8(const int8_t *xq, const float *sx, const int8_t *wq, const flo
     return REF_OK;
 }
 
+/* linear_w8a16 (docs.rs ftts_kernels::int8, linear_w8a16: f32 activations
+ * times a QuantizedMatrix, f32 out) as the tolerance reference:
+ *   y64[m][n] = sw[n] * sum_k x[m][k] * q[n][k]   in double (every product exact),
+ *   abs64     = |sw[n]| * sum_k |x[m][k] * q[n][k]|. */
+int ref_linear_w8a16_exact(const float *x, const int8_t *wq, const float *sw, double *y64, double *abs64,
+                           int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return REF_EINVAL;
+    if (M == 0 || N == 0) return REF_OK;
+    if (!y64 || !sw || (K > 0 && (!x || !wq))) return REF_EINVAL;
+    const int64_t Nd = rows_done(N);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < Nd; ++n) {
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = (double)x[m * K + k] * (double)wq[n * K + k];
+                acc += p;
+                aacc += fabs(p);
+            }
+#if MUT(8)
+            const double swn = 1.0;
+#elif MUT(7)
+            const double swn = (double)sw[m < N ? m : N - 1];
+#else
+            const double swn = (double)sw[n];
+#endif
+            y64[m * N + n] = swn * acc;
+            if (abs64) abs64[m * N + n] = fabs(swn) * aacc;
+        }
+    return REF_OK;
+}
+
 int ref_linear_w8a32(const float *x, const int8_t *wq, const float *s, float *y,
                      int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0 || K < 0) return REF_EINVAL;

@@ -345,6 +345,35 @@ def pin_shape_errors(o):
     assert st(0, 2, 4, 2) == REF_OK
 
 
+# ---------------------------------------------------------------- linear_w8a16
+
+def pin_w8a16_hand_example(o):
+    """The printed W8A32 hand example ("Fused int4 ..." section 3): f32 x times
+    int8 codes with one scale per row gives [-13, 5]; exact in double."""
+    g = load_kv("hand_example_q8.txt")
+    x = np.array(g["x"], np.float32).reshape(1, 4)
+    wq = np.array(g["codes"], np.int8).reshape(2, 4)
+    s = np.array(g["scales"], np.float32)
+    y, a = o.linear_w8a16_exact(x, wq, s)
+    assert np.array_equal(y, np.array([g["y"]], np.float64)), y
+    assert np.array_equal(a, np.array([[0.5 * (1 + 4 + 9 + 32), 0.25 * (7 + 0 + 3 + 16)]])), a
+
+
+def pin_w8a16_random(o):
+    """Random f32 x and int8 codes (every value) against a float64 matmul, and
+    against the pages' f32 order (ref_linear_w8a32) within f32 accumulation error."""
+    M, N, K = 3, 29, 300
+    x = synth.activations_f32(720, M, K)
+    wq = synth.raw_bytes(721, N * K).view(np.int8).reshape(N, K)
+    sw = (synth.uniform01(722, N) * 0.01 + 1e-3).astype(np.float32)
+    y, a = o.linear_w8a16_exact(x, wq, sw)
+    want = (x.astype(np.float64) @ wq.astype(np.float64).T) * sw[None, :].astype(np.float64)
+    assert np.allclose(y, want, rtol=1e-12, atol=1e-12)
+    assert np.allclose(a, np.abs(x.astype(np.float64)) @ np.abs(wq.astype(np.float64)).T * sw[None, :])
+    y32 = o.linear_w8a32(x, wq, sw).astype(np.float64)
+    assert np.all(np.abs(y32 - y) <= K * 2.0 ** -23 * a + 1e-30)
+
+
 # ---------------------------------------------------------------- grouped asymmetric W4A8
 
 def np_dequant_q4_group(w, s, z, K: int, G: int) -> np.ndarray:

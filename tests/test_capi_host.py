@@ -155,3 +155,14 @@ def test_linear_q4_group_validation(lib):
     assert f(1, 2, 4, 2, z=None) == lib.W4_EINVAL  # zero points required
     assert lib.workspace_bytes(lib.OP_LINEAR_Q4_GROUP, 1, 2048, 2048, 128) == 0
     assert lib.workspace_bytes(lib.OP_LINEAR_Q4_GROUP, 2048, 2048, 2048, 128) > 0
+
+
+def test_linear_w8a16_validation(lib):
+    r = lib.raw
+    f = lambda M, N, K, y=FAKE, x=FAKE: r.w4_linear_w8a16(x, FAKE, FAKE, y, M, N, K, None, 0, 0, None)
+    assert f(-1, 4, 4) == lib.W4_EINVAL
+    assert f(0, 4, 4) == lib.W4_OK
+    assert f(1, 4, 4, y=None) == lib.W4_EINVAL
+    assert f(1, 4, 4, x=None) == lib.W4_EINVAL
+    assert lib.workspace_bytes(lib.OP_LINEAR_W8A16, 1, 2048, 2048) == 0
+    assert lib.workspace_bytes(lib.OP_LINEAR_W8A16, 2048, 2048, 2048) == 2048 * 2048 * 2

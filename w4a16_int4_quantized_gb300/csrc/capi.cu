@@ -71,7 +71,7 @@ w4_status run_linear(w4::LinearArgs &a, cudaStream_t st) {
     w4::LinearArgs s16 = a;
     s16.M = 16;
     if (a.M > 16 && w4::gemv_supported(s16)) {
-        const size_t xrow = (size_t)a.K * (a.kind == w4::KIND_W4A16 ? 2 : 1);
+        const size_t xrow = (size_t)a.K * (a.kind == w4::KIND_W4A16 ? 2 : a.kind == w4::KIND_W8A16 ? 4 : 1);
         for (int64_t m0 = 0; m0 < a.M; m0 += 16) {
             w4::LinearArgs sl = a;
             sl.M = std::min<int64_t>(16, a.M - m0);
@@ -190,6 +190,23 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
     return run_linear(a, as_stream(stream));
 }
 
+w4_status w4_linear_w8a16(const float *x, const int8_t *w, const float *sw, float *y, int64_t M, int64_t N,
+                          int64_t K, void *workspace, size_t ws_bytes, uint32_t flags, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y || !sw || (K > 0 && (!x || !w))) return W4_EINVAL;
+    const w4_status ws = check_workspace(W4_OP_LINEAR_W8A16, M, N, K, 0, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), as_stream(stream)));
+    w4::LinearArgs a = {};
+    a.kind = w4::KIND_W8A16;
+    a.x = x; a.w = reinterpret_cast<const uint8_t *>(w); a.scale = sw; a.sx = nullptr; a.y = y;
+    a.M = M; a.N = N; a.K = K; a.G = 0; a.layout = W4_LAYOUT_ROWMAJOR; a.flags = flags;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    return run_linear(a, as_stream(stream));
+}
+
 w4_status w4_linear_q4_group(const int8_t *xq, const float *sx, const uint8_t *w, const uint16_t *scales_f16,
                              const uint8_t *zeros, float *y, int64_t M, int64_t N, int64_t K, int64_t G,
                              int32_t layout, void *workspace, size_t ws_bytes, uint32_t flags, void *stream) {
@@ -267,6 +284,7 @@ size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G
         case W4_OP_LINEAR_Q8: return w4::gemm_workspace_bytes(w4::KIND_W8A8, M, N, K, G);
         case W4_OP_LINEAR_W4A16: return w4::gemm_workspace_bytes(w4::KIND_W4A16, M, N, K, G);
         case W4_OP_LINEAR_Q4_GROUP: return w4::gemm_workspace_bytes(w4::KIND_W4A8G, M, N, K, G);
+        case W4_OP_LINEAR_W8A16: return w4::gemm_workspace_bytes(w4::KIND_W8A16, M, N, K, G);
         default: return 0;
     }
 }

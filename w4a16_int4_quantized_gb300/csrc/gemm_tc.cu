@@ -208,6 +208,21 @@ W4_DEV uint4 conv_w4a8(uint32_t w) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 8 int8 (two words) -> 8 bf16 of the same integers (exact), natural order.
+W4_DEV uint4 conv_w8a16(uint32_t lo, uint32_t hi) {
+    const uint32_t wd[2] = {lo, hi};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t w = wd[e >> 1];
+        const int a = (int)(int8_t)((w >> (16 * (e & 1))) & 0xFFu);
+        const int b = (int)(int8_t)((w >> (16 * (e & 1) + 8)) & 0xFFu);
+        __nv_bfloat162 h = __floats2bfloat162_rn((float)a, (float)b);
+        o[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // 8 int8 (two words) -> 8 f16 of the same integers, natural order.
 W4_DEV uint4 conv_w8a8(uint32_t lo, uint32_t hi) {
     const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6480), __ushort_as_half((unsigned short)0x6480));
@@ -232,14 +247,14 @@ W4_DEV uint4 conv_w8a8(uint32_t lo, uint32_t hi) {
 // the interleave with 4x4 byte transposes before the same dequantisation.
 template <int KIND, bool IL>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
-    constexpr bool kW4 = KIND != KIND_W8A8;
+    constexpr bool kW4 = KIND != KIND_W8A8 && KIND != KIND_W8A16;
     static_assert(!IL || kW4, "the interleaved layout holds int4 only");
     constexpr int kPRow = kW4 ? 32 : 64;             // packed bytes per weight row per stage
     constexpr int kATile = kBM * 128;                // 16 KB
     constexpr int kBTile = kBN * 128;                // 32 KB
     constexpr int kPTile = kBM * kPRow;              // 4 | 8 KB
     constexpr uint32_t kStageTx = kBTile + kPTile;
-    constexpr uint32_t kIdesc = idesc_f16(KIND == KIND_W4A16 ? 1u : 0u, kBM, kBN);
+    constexpr uint32_t kIdesc = idesc_f16((KIND == KIND_W4A16 || KIND == KIND_W8A16) ? 1u : 0u, kBM, kBN);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -428,14 +443,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             if (!wait_or_abort(&sh->tma_full[s], (g / kStages) & 1, sh, p.status)) break;
             const uint8_t *prow = p_tiles + s * kPTile + row * kPRow;
             uint8_t *arow = a_row + s * kATile;
-            if constexpr (KIND == KIND_W8A8) {
+            if constexpr (!kW4) {
                 const uint4 q0 = *reinterpret_cast<const uint4 *>(prow + 32 * half);
                 const uint4 q1 = *reinterpret_cast<const uint4 *>(prow + 32 * half + 16);
                 const uint32_t wds[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int chunk = 4 * half + c;
-                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ rr) << 4)) = conv_w8a8(wds[2 * c], wds[2 * c + 1]);
+                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ rr) << 4)) =
+                        KIND == KIND_W8A16 ? conv_w8a16(wds[2 * c], wds[2 * c + 1]) : conv_w8a8(wds[2 * c], wds[2 * c + 1]);
                 }
             } else {
                 const uint4 pk = *reinterpret_cast<const uint4 *>(prow + 16 * half);
@@ -474,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tc_fence_after();
             const int nrow = n0 + 32 * q + lane;
             float swn = 1.0f;
-            if constexpr (KIND == KIND_W4A8 || KIND == KIND_W8A8) swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
+            if constexpr (KIND == KIND_W4A8 || KIND == KIND_W8A8 || KIND == KIND_W8A16)
+                swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
 #pragma unroll 1
             for (int cc = 0; cc < kBN / 64; ++cc) {
                 const int col0 = (kBN / 2) * hc + 32 * cc;
@@ -488,13 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 // sx of the chunk's 32 activation rows: one coalesced load, then shuffles
                 float sxl = 0.0f;
-                if constexpr (KIND != KIND_W4A16) sxl = (m0 + col0 + lane < p.M) ? p.sx[m0 + col0 + lane] : 0.0f;
+                if constexpr (KIND != KIND_W4A16 && KIND != KIND_W8A16)
+                    sxl = (m0 + col0 + lane < p.M) ? p.sx[m0 + col0 + lane] : 0.0f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {  // every lane takes part in the shuffles
                     const int m = m0 + col0 + j;
                     float out = __uint_as_float(v[j]);
                     if constexpr (KIND == KIND_W4A8G)
                         out = __fmul_rn(out, __shfl_sync(0xffffffffu, sxl, j));  // sx * sum_g acc_g * s_g
+                    else if constexpr (KIND == KIND_W8A16)
+                        out = __fmul_rn(out, swn);  // sw * sum x q
                     else if constexpr (KIND != KIND_W4A16)
                         out = __fmul_rn(__fmul_rn(out, __shfl_sync(0xffffffffu, sxl, j)), swn);
                     // streaming store: y is written once, the operand tiles stay in L2
@@ -530,8 +550,26 @@ __global__ void s8_to_f16_kernel(const int8_t *__restrict__ x, uint16_t *__restr
     }
 }
 
+// f32 activations [M][K] -> bf16 [M][Kx] (round to nearest even, zero padded).
+__global__ void f32_to_bf16_kernel(const float *__restrict__ x, uint16_t *__restrict__ out, int64_t M, int64_t K,
+                                   int64_t Kx) {
+    const int64_t groups = M * (Kx / 8);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < groups; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / (Kx / 8), k = (i - m * (Kx / 8)) * 8;
+        uint32_t h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = (k + 2 * e < K) ? x[m * K + k + 2 * e] : 0.0f;
+            const float b = (k + 2 * e + 1 < K) ? x[m * K + k + 2 * e + 1] : 0.0f;
+            __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+            h[e] = *reinterpret_cast<uint32_t *>(&v);
+        }
+        *reinterpret_cast<uint4 *>(out + m * Kx + k) = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+}
+
 constexpr int smem_bytes(int kind) {
-    return 1024 + kStages * (kBM * 128 + kBN * 128 + kBM * (kind == KIND_W8A8 ? 64 : 32)) + 1024;
+    return 1024 + kStages * (kBM * 128 + kBN * 128 + kBM * ((kind == KIND_W8A8 || kind == KIND_W8A16) ? 64 : 32)) + 1024;
 }
 
 template <int KIND, bool IL>
@@ -563,16 +601,16 @@ bool gemm_supported(const LinearArgs &a) {
     if (a.kind == KIND_W4A8G && (a.layout != W4_LAYOUT_ROWMAJOR || a.G % 32)) return false;
     if (a.layout == W4_LAYOUT_N64) {
         // [N/64][K][32 B]: rows of 32 bytes, any K; W4A16 groups of whole 32-column chunks
-        if (a.kind == KIND_W8A8 || a.N % 64) return false;
+        if (a.kind == KIND_W8A8 || a.kind == KIND_W8A16 || a.N % 64) return false;
         if (a.kind == KIND_W4A16 && a.G % 32) return false;
     } else {
-        const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
+        const int64_t Kb = (a.kind == KIND_W8A8 || a.kind == KIND_W8A16) ? a.K : (a.K + 1) / 2;
         if (Kb % 16) return false;  // TMA row stride
     }
     if (a.kind == KIND_W4A16) {
         if (a.K % 8 || a.G % 8) return false;  // bf16 rows for TMA; one scale per 8 columns
         if (reinterpret_cast<uintptr_t>(a.x) % 16) return false;
-    } else if (a.kind != KIND_W4A8G) {
+    } else if (a.kind == KIND_W4A8 || a.kind == KIND_W8A8) {
         // exact integer accumulation in f32 needs 127 * max|q| * K < 2^24
         if (a.K > (a.kind == KIND_W4A8 ? 16384 : 1024)) return false;
     }
@@ -608,8 +646,12 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
         if (!a.workspace || a.ws_bytes < need) return cudaErrorInvalidValue;
         const int64_t groups = a.M * (Kx / 8);
         const int64_t blocks = std::min<int64_t>(ceil_div(groups, 256), 152 * 8);
-        s8_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const int8_t *>(a.x),
-                                                           static_cast<uint16_t *>(a.workspace), a.M, a.K, Kx);
+        if (a.kind == KIND_W8A16)  // f32 activations -> bf16 (the prefill's one rounding of x)
+            f32_to_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float *>(a.x),
+                                                                 static_cast<uint16_t *>(a.workspace), a.M, a.K, Kx);
+        else
+            s8_to_f16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const int8_t *>(a.x),
+                                                               static_cast<uint16_t *>(a.workspace), a.M, a.K, Kx);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         xsrc = a.workspace;
@@ -621,7 +663,8 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
         const uint64_t dims[2] = {(uint64_t)Kx, (uint64_t)a.M};
         const uint64_t strides[1] = {(uint64_t)Kx * 2};
         const uint32_t box[2] = {(uint32_t)kBK, (uint32_t)kBN};
-        if (!encode_tmap(&p.xmap, a.kind == KIND_W4A16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+        if (!encode_tmap(&p.xmap, (a.kind == KIND_W4A16 || a.kind == KIND_W8A16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          2, xsrc, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
     }
@@ -635,10 +678,11 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     } else {
-        const int64_t Kb = (a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2;
+        const bool w8 = a.kind == KIND_W8A8 || a.kind == KIND_W8A16;
+        const int64_t Kb = w8 ? a.K : (a.K + 1) / 2;
         const uint64_t dims[2] = {(uint64_t)Kb, (uint64_t)a.N};
         const uint64_t strides[1] = {(uint64_t)Kb};
-        const uint32_t box[2] = {(uint32_t)(a.kind == KIND_W8A8 ? 64 : 32), (uint32_t)kBM};
+        const uint32_t box[2] = {(uint32_t)(w8 ? 64 : 32), (uint32_t)kBM};
         if (!encode_tmap(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
@@ -647,6 +691,7 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
         case KIND_W4A16: return il ? launch_kernel<KIND_W4A16, true>(p, st) : launch_kernel<KIND_W4A16, false>(p, st);
         case KIND_W4A8: return il ? launch_kernel<KIND_W4A8, true>(p, st) : launch_kernel<KIND_W4A8, false>(p, st);
         case KIND_W4A8G: return launch_kernel<KIND_W4A8G, false>(p, st);
+        case KIND_W8A16: return launch_kernel<KIND_W8A16, false>(p, st);
         default: return launch_kernel<KIND_W8A8, false>(p, st);
     }
 }

@@ -52,6 +52,8 @@ namespace {
 template <int KIND> constexpr bool kGrouped = KIND == KIND_W4A16 || KIND == KIND_W4A8G;  // f16 group scales
 template <int KIND> constexpr bool kIntAcc = KIND == KIND_W4A8 || KIND == KIND_W8A8;     // i32 accumulators
 template <int KIND> constexpr bool kBiased = KIND == KIND_W4A8 || KIND == KIND_W4A8G;    // u - 8 MMA operands
+template <int KIND> constexpr bool kW8 = KIND == KIND_W8A8 || KIND == KIND_W8A16;        // int8 weights, 32-B chunks
+template <int KIND> constexpr int kXPlanes = KIND == KIND_W8A16 ? 2 : 1;  // f32 x as bf16 hi + lo
 
 struct GemvParams {
     const void *x;
@@ -86,13 +88,6 @@ W4_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint3
     asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-W4_DEV void mma_s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 "
-        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
@@ -143,6 +138,19 @@ W4_DEV void s8_to_f16_pairs(uint32_t lo, uint32_t hi, const uint32_t (&sel)[4], 
     }
 }
 
+// Eight int8 values -> four bf16x2 pairs of the same integers (exact: |b| <= 128
+// fits bf16's 8-bit significand), pair i from the bytes PRMT selector sel[i]
+// puts in result bytes 0 and 2.
+W4_DEV void s8_to_bf16_pairs(uint32_t lo, uint32_t hi, const uint32_t (&sel)[4], uint32_t (&p)[4]) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t v = prmt(lo, hi, sel[i]);  // bytes 0 and 2 hold the two values
+        const int a = (int)(int8_t)(v & 0xFFu), b = (int)(int8_t)((v >> 16) & 0xFFu);
+        __nv_bfloat162 h = __floats2bfloat162_rn((float)a, (float)b);
+        p[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
 W4_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
     asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -167,13 +175,13 @@ W4_DEV int fast_div(int j, uint32_t magic) { return (int)__umulhi((uint32_t)j, m
 template <bool SWZ, int KIND>
 W4_DEV int wword_off(int c, int g, int t, int R128) {
     if constexpr (SWZ) {
-        if constexpr (KIND == KIND_W8A8) {
+        if constexpr (kW8<KIND>) {
             const int c16 = 2 * c + (t >> 1);
             return (c16 >> 3) * R128 + (((c16 & 7) ^ g) << 4) + 8 * (t & 1);
         }
         return (c >> 3) * R128 + (((c & 7) ^ g) << 4) + 4 * t;
     } else {
-        return (KIND == KIND_W8A8) ? 32 * c + 8 * t : 16 * c + 4 * t;
+        return kW8<KIND> ? 32 * c + 8 * t : 16 * c + 4 * t;
     }
 }
 
@@ -183,7 +191,8 @@ W4_DEV int wword_off(int c, int g, int t, int R128) {
 // of the tile; xr[mt]: the thread's activations of the unit's first chunk.
 template <int KIND, bool SWZ, int RB, int MT, int CPG>
 W4_DEV void unit_mma(const uint8_t *w0, const uint8_t *w8, int c0, int g, int t, int R128,
-                     const uint8_t *const (&xr)[MT], const bool (&xvalid)[MT], int cpg_rt, float (&part)[MT][4]) {
+                     const uint8_t *const (&xr)[MT], const bool (&xvalid)[MT], int cpg_rt, float (&part)[MT][4],
+                     int xlo = 0) {
     const uint32_t xsel8[4] = {0x0100u, 0x0302u, 0x0504u, 0x0706u};
     const int nc = CPG > 0 ? CPG : cpg_rt;
 #pragma unroll
@@ -197,6 +206,13 @@ W4_DEV void unit_mma(const uint8_t *w0, const uint8_t *w8, int c0, int g, int t,
             } else if constexpr (kBiased<KIND>) {
                 unpack_biased_f16(*reinterpret_cast<const uint32_t *>(w0 + wo), pa);
                 if (RB == 16) unpack_biased_f16(*reinterpret_cast<const uint32_t *>(w8 + wo), pb);
+            } else if constexpr (KIND == KIND_W8A16) {
+                const uint2 wa = *reinterpret_cast<const uint2 *>(w0 + wo);
+                s8_to_bf16_pairs(wa.x, wa.y, xsel8, pa);
+                if (RB == 16) {
+                    const uint2 wb = *reinterpret_cast<const uint2 *>(w8 + wo);
+                    s8_to_bf16_pairs(wb.x, wb.y, xsel8, pb);
+                }
             } else {
                 const uint2 wa = *reinterpret_cast<const uint2 *>(w0 + wo);
                 s8_to_f16_pairs(wa.x, wa.y, xsel8, pa);
@@ -213,6 +229,14 @@ W4_DEV void unit_mma(const uint8_t *w0, const uint8_t *w8, int c0, int g, int t,
                 if constexpr (KIND == KIND_W4A16) {
                     mma_bf16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
                     mma_bf16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+                } else if constexpr (KIND == KIND_W8A16) {
+                    // x = hi + lo (two bf16 planes): two MMA pairs into the same f32 partial
+                    uint4 xl = make_uint4(0u, 0u, 0u, 0u);
+                    if (xvalid[mt]) xl = *reinterpret_cast<const uint4 *>(xr[mt] + xlo + 64 * cc);
+                    mma_bf16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
+                    mma_bf16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
+                    mma_bf16(part[mt], pa[0], pb[0], pa[1], pb[1], xl.x, xl.y);
+                    mma_bf16(part[mt], pa[2], pb[2], pa[3], pb[3], xl.z, xl.w);
                 } else {
                     mma_f16(part[mt], pa[0], pb[0], pa[1], pb[1], xv.x, xv.y);
                     mma_f16(part[mt], pa[2], pb[2], pa[3], pb[3], xv.z, xv.w);
@@ -274,7 +298,32 @@ W4_DEV void stage_x(const GemvParams &p, int k0, int span_k, int nthr, uint8_t *
             const int m = fast_div(j, pr_magic), b8 = j - m * per_row;
             const int kk = k0 + 8 * b8;
             uint4 o;
-            if constexpr (kInt) {
+            if constexpr (KIND == KIND_W8A16) {
+                // f32 x -> bf16 hi = rn(x), lo = rn(x - hi), pairs (x0 x1)(x2 x3)(x4 x5)(x6 x7)
+                const float *xr = static_cast<const float *>(p.x) + (size_t)m * p.K;
+                float e[8];
+                if (p.x_vec && kk + 8 <= p.K) {
+                    const float4 a0 = __ldg(reinterpret_cast<const float4 *>(xr + kk));
+                    const float4 a1 = __ldg(reinterpret_cast<const float4 *>(xr + kk + 4));
+                    e[0] = a0.x; e[1] = a0.y; e[2] = a0.z; e[3] = a0.w;
+                    e[4] = a1.x; e[5] = a1.y; e[6] = a1.z; e[7] = a1.w;
+                } else {
+#pragma unroll
+                    for (int i2 = 0; i2 < 8; ++i2) e[i2] = (kk + i2 < p.K) ? xr[kk + i2] : 0.0f;
+                }
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(e[2 * q], e[2 * q + 1]);
+                    const float2 hf = __bfloat1622float2(h);
+                    const __nv_bfloat162 l = __floats2bfloat162_rn(e[2 * q] - hf.x, e[2 * q + 1] - hf.y);
+                    hi[q] = *reinterpret_cast<const uint32_t *>(&h);
+                    lo[q] = *reinterpret_cast<const uint32_t *>(&l);
+                }
+                *reinterpret_cast<uint4 *>(smem + p.x_off + (p.M + m) * p.xstride + 16 * b8) =
+                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                o = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            } else if constexpr (kInt) {
                 const int8_t *xr = static_cast<const int8_t *>(p.x) + (size_t)m * p.K;
                 uint2 v;
                 if (p.x_vec && kk + 8 <= p.K) {
@@ -419,6 +468,8 @@ W4_DEV void combine_and_store(const GemvParams &p, Acc (&acc)[MT][4], int wr, in
                 out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[mt][i]), p.sx[m]), sw);
             } else if constexpr (KIND == KIND_W4A8G) {
                 out = __fmul_rn((float)acc[mt][i], p.sx[m]);  // sx * sum_g acc_g * s_g
+            } else if constexpr (KIND == KIND_W8A16) {
+                out = __fmul_rn((float)acc[mt][i], static_cast<const float *>(p.scale)[n]);  // sw * sum x q
             } else {
                 out = (float)acc[mt][i];
             }
@@ -493,7 +544,6 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     const int k0 = u0 * p.unit_k;
     const int span_k = nun * p.unit_k;
     const int span_bytes = nun * p.unit_bytes;
-    constexpr bool kInt = KIND != KIND_W4A16;
     const int rows = min(p.R, p.N - row0);
     const int nthr = blockDim.x;
 
@@ -616,6 +666,11 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
                 acc[mt][2] = fmaf(s1, (float)(__float2int_rn(part[mt][2]) + c1 * xa), acc[mt][2]);
                 acc[mt][3] = fmaf(s1, (float)(__float2int_rn(part[mt][3]) + c1 * xb), acc[mt][3]);
             }
+        } else if constexpr (KIND == KIND_W8A16) {
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[mt][i] += part[mt][i];
         } else if constexpr (KIND == KIND_W4A16) {
             const float s0 = sc0[u];
             const float s1 = (RB == 16) ? sc1[u] : 0.0f;
@@ -641,7 +696,8 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
         const uint8_t *xr[MT];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) xr[mt] = xrow[mt] + 64 * cpg * u;
-        unit_mma<KIND, false, RB, MT, CPG>(wrow, wrow8, cpg * ul, g, t, R128, xr, xvalid, cpg, part);
+        unit_mma<KIND, false, RB, MT, CPG>(wrow, wrow8, cpg * ul, g, t, R128, xr, xvalid, cpg, part,
+                                           p.M * p.xstride);
     };
 
     // Units are processed in phases (one phase for the row-major layout); a
@@ -841,7 +897,14 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
             const uint8_t b = p.w[((n >> 6) * p.K + k) * 32 + ((n & 63) & 31)];
             return ((n & 63) < 32) ? (b & 0xFu) : (b >> 4);
         };
-        if constexpr (KIND == KIND_W4A8G) {
+        if constexpr (KIND == KIND_W8A16) {
+            const float *xr = static_cast<const float *>(p.x) + m * p.K;
+            float acc = 0.0f;
+            for (int64_t k = lane; k < p.K; k += 32) acc = fmaf(xr[k], (float)reinterpret_cast<const int8_t *>(p.w)[n * p.K + k], acc);
+#pragma unroll
+            for (int sft = 16; sft; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+            if (lane == 0) p.y[m * p.N + n] = __fmul_rn(acc, static_cast<const float *>(p.scale)[n]);
+        } else if constexpr (KIND == KIND_W4A8G) {
             const int8_t *xr = static_cast<const int8_t *>(p.x) + m * p.K;
             const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
             const int64_t G = p.unit_k;
@@ -1001,8 +1064,8 @@ constexpr int kMinTiles = 128;  // CTAs (of 8 rows) below which K is split acros
 // Fills the unit geometry of p for the call; false when the fast path cannot describe it.
 bool geometry(const LinearArgs &a, GemvParams &p) {
     const int64_t Kp = a.K + (a.K & 1);
-    p.Kb = (int)((a.kind == KIND_W8A8) ? a.K : (a.K + 1) / 2);
-    if (a.kind == KIND_W8A8) {
+    p.Kb = (int)((a.kind == KIND_W8A8 || a.kind == KIND_W8A16) ? a.K : (a.K + 1) / 2);
+    if (a.kind == KIND_W8A8 || a.kind == KIND_W8A16) {
         if (a.K % 32) return false;
         p.cpg = 1; p.unit_k = 32; p.unit_bytes = 32; p.units = (int)(a.K / 32); p.ng = 0;
     } else if (a.kind == KIND_W4A8) {
@@ -1026,7 +1089,8 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_ti
     p.WK = s.WK;
     const int span_k = p.upc * p.unit_k;
     const int tile_units = n64 ? p.upp : p.upc;
-    p.wstride = pad_to(tile_units * p.unit_bytes, (a.kind == KIND_W8A8) ? 32 : 16);
+    const bool w8 = a.kind == KIND_W8A8 || a.kind == KIND_W8A16;
+    p.wstride = pad_to(tile_units * p.unit_bytes, w8 ? 32 : 16);
     p.xstride = pad_to(span_k * 2, 64);  // staged as 16-bit pairs for every kind
     p.sstride = p.upc | 1;  // f32 scales per row, odd so the 8 rows of a warp hit 8 banks
     int off = 0;
@@ -1035,7 +1099,7 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_ti
     p.w_off = off;
     if (weight_tile) off += (int)round_up((int64_t)p.R * p.wstride, 128);
     p.x_off = off;
-    off += (int)round_up((int64_t)a.M * p.xstride, 128);
+    off += (int)round_up((int64_t)a.M * p.xstride * (a.kind == KIND_W8A16 ? 2 : 1), 128);
     p.sc_off = off;
     const bool grouped = a.kind == KIND_W4A16 || a.kind == KIND_W4A8G;
     if (grouped) off += (int)round_up((int64_t)p.R * p.sstride * 4, 128);
@@ -1057,7 +1121,7 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_ti
 bool gemv_supported(const LinearArgs &a) {
     if (a.M > 16 || a.M < 1) return false;
     if (a.N > 0x3FFFFFFF || a.K > 0x7FFFFFF) return false;
-    if (a.kind == KIND_W8A8 && a.layout != W4_LAYOUT_ROWMAJOR) return false;
+    if ((a.kind == KIND_W8A8 || a.kind == KIND_W8A16) && a.layout != W4_LAYOUT_ROWMAJOR) return false;
     GemvParams p = {};
     if (!geometry(a, p)) return false;
     if ((reinterpret_cast<uintptr_t>(a.w) % 16) != 0) return false;
@@ -1077,7 +1141,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     p.M = (int)a.M;
     p.N = (int)a.N;
     p.K = (int)a.K;
-    const int esize = (a.kind == KIND_W4A16) ? 2 : 1;
+    const int esize = (a.kind == KIND_W4A16) ? 2 : (a.kind == KIND_W8A16) ? 4 : 1;
     const bool n64 = a.layout == W4_LAYOUT_N64;
 
     // The K split (warps per CTA along K, cluster ranks along K) depends only
@@ -1154,6 +1218,8 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
                        : dispatch_rb_mt<KIND_W4A8, false, 1>(p, s, threads, smem, st, pdl);
         case KIND_W8A8:
             return dispatch_rb_mt<KIND_W8A8, false, 1>(p, s, threads, smem, st, pdl);
+        case KIND_W8A16:
+            return dispatch_rb_mt<KIND_W8A16, false, 1>(p, s, threads, smem, st, pdl);
         case KIND_W4A8G:
             return n64 ? dispatch_grouped<KIND_W4A8G, true>(p, s, threads, smem, st, pdl)
                        : dispatch_grouped<KIND_W4A8G, false>(p, s, threads, smem, st, pdl);
@@ -1186,6 +1252,7 @@ cudaError_t launch_generic(const LinearArgs &a, cudaStream_t st) {
         case KIND_W4A8: generic_kernel<KIND_W4A8><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
         case KIND_W8A8: generic_kernel<KIND_W8A8><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
         case KIND_W4A8G: generic_kernel<KIND_W4A8G><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
+        case KIND_W8A16: generic_kernel<KIND_W8A16><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
         default: generic_kernel<KIND_W4A16><<<(unsigned)blocks, 256, 0, st>>>(p, a.layout); break;
     }
     return cudaGetLastError();

@@ -11,13 +11,14 @@
 namespace w4 {
 
 // W4A8G: grouped asymmetric W4A8 (per-group f16 scales and zero points).
-enum Kind : int { KIND_W4A8 = 0, KIND_W8A8 = 1, KIND_W4A16 = 2, KIND_W4A8G = 3 };
+// W8A16: int8 weights with f32 channel scales, f32 activations.
+enum Kind : int { KIND_W4A8 = 0, KIND_W8A8 = 1, KIND_W4A16 = 2, KIND_W4A8G = 3, KIND_W8A16 = 4 };
 
 // One linear call after host validation (shapes legal, pointers non-NULL,
 // M, N, K > 0).
 struct LinearArgs {
     int kind;
-    const void *x;       // int8 [M][K] (W4A8, W8A8) or bf16 [M][K] (W4A16)
+    const void *x;       // int8 [M][K] (W4A8, W8A8, W4A8G), bf16 [M][K] (W4A16) or f32 [M][K] (W8A16)
     const uint8_t *w;    // packed int4 (layout) or int8 [N][K]
     const void *scale;   // f32 sw [N] (W4A8, W8A8) or f16 [N][Kp/G] (W4A16, W4A8G)
     const uint8_t *zeros;  // W4A8G: zero points [N][Kp/G]

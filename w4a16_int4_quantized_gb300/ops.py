@@ -22,7 +22,7 @@ LIB_PATH = os.path.join(_HERE, "libw4gb300.so")
 W4_OK, W4_EINVAL, W4_ESHAPE, W4_ECUDA = 0, 1, 2, 3
 LAYOUT_ROWMAJOR, LAYOUT_N64 = 0, 1
 FLAG_PDL = 1
-OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16, OP_LINEAR_Q4_GROUP = 0, 1, 2, 3
+OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16, OP_LINEAR_Q4_GROUP, OP_LINEAR_W8A16 = 0, 1, 2, 3, 4
 CHAIN_MAX_LINEARS, CHAIN_MAX_K = 64, 8192
 
 
@@ -43,6 +43,7 @@ SIGNATURES = [
     ("w4_linear_q8", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_noalloc", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
+    ("w4_linear_w8a16", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_group", _i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_chain_q4", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
     ("w4_chain_workspace_bytes", _sz, [_vp, _i32, _i32]),
@@ -211,6 +212,17 @@ def linear_w4a16_group(x, w, scales, G: int, K: int | None = None, N: int | None
     ws, wsb = _workspace(OP_LINEAR_W4A16, M, N, K, G, workspace, x.device)
     _check(raw.w4_linear_w4a16_group(_ptr(x), _ptr(w), _ptr(scales), _ptr(y), M, N, K, G, layout,
                                      _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_w4a16_group")
+    return y
+
+
+def linear_w8a16(x, w, sw, flags: int = 0, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """W8A16: y[M, N] = sw[n] * sum_k x[m, k] * q[n, k], x f32, q int8."""
+    M, K = x.shape
+    N = sw.numel()
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(OP_LINEAR_W8A16, M, N, K, 0, workspace, x.device)
+    _check(raw.w4_linear_w8a16(_ptr(x), _ptr(w), _ptr(sw), _ptr(y), M, N, K, _ptr(ws), wsb, flags, _stream(stream)),
+           "w4_linear_w8a16")
     return y
 
 
