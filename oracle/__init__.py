@@ -99,6 +99,10 @@ class Oracle:
         L.ref_linear_w4a16_exact.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64]
         L.ref_linear_w8a16_exact.restype = i32
         L.ref_linear_w8a16_exact.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64]
+        L.ref_blocks_b32.restype = i32
+        L.ref_blocks_b32.argtypes = [vp, vp, vp, i64, i64]
+        L.ref_linear_w4a16_b32_exact.restype = i32
+        L.ref_linear_w4a16_b32_exact.argtypes = [vp, vp, vp, vp, i64, i64, i64]
         L.ref_linear_q4_group.restype = i32
         L.ref_linear_q4_group.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64]
         L.ref_linear_w4a16_lanes.restype = i32
@@ -240,6 +244,26 @@ class Oracle:
         y = np.zeros((M, N), np.float64)
         a = np.zeros((M, N), np.float64)
         rc = self.lib.ref_linear_w8a16_exact(_p(x), _p(wq), _p(sw), _p(y), _p(a), M, N, K)
+        assert rc == REF_OK, rc
+        return y, a
+
+    def blocks_b32(self, w, s, K: int):
+        w = np.ascontiguousarray(w, dtype=np.uint8)
+        s = np.ascontiguousarray(s, dtype=np.uint16)
+        N = w.shape[0]
+        nb = (K + (K & 1)) // 32
+        out = np.zeros((N, nb * 18), np.uint8)
+        rc = self.lib.ref_blocks_b32(_p(w), _p(s), _p(out), N, int(K))
+        assert rc == REF_OK, rc
+        return out
+
+    def linear_w4a16_b32_exact(self, x, blocks, K: int):
+        x = np.ascontiguousarray(x, dtype=np.uint16)
+        blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
+        M, N = x.shape[0], blocks.shape[0]
+        y = np.zeros((M, N), np.float64)
+        a = np.zeros((M, N), np.float64)
+        rc = self.lib.ref_linear_w4a16_b32_exact(_p(x), _p(blocks), _p(y), _p(a), M, N, int(K))
         assert rc == REF_OK, rc
         return y, a
 

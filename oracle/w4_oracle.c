@@ -495,6 +495,65 @@ int ref_linear_q4_group(const int8_t *xq, const float *sx, const uint8_t *w, con
     return REF_OK;
 }
 
+/* Inline-scale block format, written from the description in "Fused int4
+ * and int8 dequantize-matmul in C" (Going further: "blocks of 32 with the scale
+ * stored inline next to the codes"): row n is nb = Kp / 32 blocks of 18 bytes,
+ * bytes 0-1 the block's f16 scale (little-endian), bytes 2-17 the signed
+ * nibbles of columns 32b .. 32b+31, low nibble = even column.  The same
+ * numbers as group-wise W4A16 with G = 32; only the bytes move. */
+int ref_blocks_b32(const uint8_t *w, const uint16_t *s, uint8_t *blocks, int64_t N, int64_t K) {
+    if (N < 0 || K < 0) return REF_EINVAL;
+    const int64_t Kp = K + (K & 1);
+    if (Kp % 32) return REF_ESHAPE;
+    if (N == 0 || K == 0) return REF_OK;
+    if (!w || !s || !blocks) return REF_EINVAL;
+    const int64_t nb = Kp / 32, Kb = Kp / 2;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t b = 0; b < nb; ++b) {
+            uint8_t *blk = blocks + (n * nb + b) * 18;
+            const uint16_t sc = s[n * nb + b];
+            blk[0] = (uint8_t)(sc & 0xFF);
+            blk[1] = (uint8_t)(sc >> 8);
+            for (int64_t j = 0; j < 16; ++j) blk[2 + j] = w[n * Kb + 16 * b + j];
+        }
+    return REF_OK;
+}
+
+/* Group-wise W4A16 read from the inline-scale blocks: every step of
+ * ref_linear_w4a16_exact (G = 32), the codes and scale of group b taken from
+ * block b of the row. */
+int ref_linear_w4a16_b32_exact(const uint16_t *x, const uint8_t *blocks, double *y64, double *abs64,
+                               int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return REF_EINVAL;
+    const int64_t Kp = K + (K & 1);
+    if (Kp % 32) return REF_ESHAPE;
+    if (M == 0 || N == 0) return REF_OK;
+    if (!y64 || (K > 0 && (!x || !blocks))) return REF_EINVAL;
+    const int64_t nb = Kp / 32;
+    const int64_t Nd = rows_done(N);
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < Nd; ++n) {
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *blk = blocks + (n * nb + b) * 18;
+                const double sg = (double)ref_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
+                double part = 0.0, apart = 0.0;
+                for (int64_t i = 0; i < 32; ++i) {
+                    const int64_t k = 32 * b + i;
+                    if (k >= K) continue;
+                    const double p = (double)act_bf16(x[m * K + k]) * (double)ref_nibble_signed(nib(blk + 2, i));
+                    part += p;
+                    apart += fabs(p);
+                }
+                acc += sg * part;
+                aacc += fabs(sg) * apart;
+            }
+            y64[m * N + n] = acc;
+            if (abs64) abs64[m * N + n] = aacc;
+        }
+    return REF_OK;
+}
+
 /* The pages' own f32 order ("Fused int4 ..." 2.4): 8 independent lanes per
  * group, lane l accumulating positions l, l+8, ... in increasing order; the
  * lanes combine in the fixed tree; the output accumulates s_g * partial_g in

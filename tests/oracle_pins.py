@@ -345,6 +345,35 @@ def pin_shape_errors(o):
     assert st(0, 2, 4, 2) == REF_OK
 
 
+# ---------------------------------------------------------------- inline-scale blocks of 32
+
+def pin_b32_closed_form(o):
+    """One block by hand: codes q_k = (k mod 16) - 8 (two runs of -8..7, sum -16),
+    scale 0.5 (f16 0x3800), x = 1: y = 0.5 * -16 = -8; the block's bytes are
+    [0x00, 0x38] then byte j = nib(2j) | nib(2j+1) << 4 of the signed codes."""
+    q = (np.arange(32) % 16) - 8
+    nibs = q & 0xF
+    codes = (nibs[0::2] | (nibs[1::2] << 4)).astype(np.uint8)
+    blk = np.concatenate([[0x00, 0x38], codes]).astype(np.uint8)[None]
+    x = np.full((1, 32), 0x3F80, np.uint16)                # bf16 1.0
+    y, a = o.linear_w4a16_b32_exact(x, blk, 32)
+    assert y[0, 0] == -8.0 and a[0, 0] == 0.5 * 2 * (8 * 9 // 2 + 7 * 8 // 2), (y, a)
+    b = o.blocks_b32(codes[None], np.array([[0x3800]], np.uint16), 32)
+    assert np.array_equal(b, blk), b
+
+
+def pin_b32_same_numbers_as_planes(o):
+    """Blocks built from the planes give exactly the plane form's W4A16 (G = 32)
+    result; odd K (pad nibble) included."""
+    for (M, N, K) in ((2, 5, 64), (1, 9, 255), (3, 4, 1024)):
+        x, w, s = synth.w4a16_inputs(730 + K, M, N, K, 32)
+        blocks = o.blocks_b32(w, s, K)
+        assert blocks.shape == (N, (K + (K & 1)) // 32 * 18)
+        y, a = o.linear_w4a16_b32_exact(x, blocks, K)
+        yp, ap = o.linear_w4a16_exact(x, w, s, K, 32)
+        assert np.array_equal(y, yp) and np.array_equal(a, ap), K
+
+
 # ---------------------------------------------------------------- linear_w8a16
 
 def pin_w8a16_hand_example(o):
