@@ -85,6 +85,11 @@ WORKLOADS = {
     "w4a8g_decode_m1_n13312": _wl("w4a8g", 1, 13312, 2048, 128, 0,
                                   "grouped asymmetric W4A8 (f16 scales + zero points per group of 128), M=1, "
                                   "K=2048, N=13312 (per-row Q8 quantize + linear)"),
+    "w4a16_b32_decode_m1_n13312": _wl("w4a16", 1, 13312, 2048, 32, 2,
+                                      "W4A16 M=1, K=2048, N=13312, inline-scale blocks of 32 (f16 scale beside "
+                                      "16 bytes of codes, 18 bytes per block)"),
+    "w4a16_b32_decode_m16_n13312": _wl("w4a16", 16, 13312, 2048, 32, 2,
+                                       "W4A16 decode batch M=16, K=2048, N=13312, inline-scale blocks of 32"),
     "w4a8g_prefill_m2048_n13312": _wl("w4a8g", 2048, 13312, 2048, 128, 0,
                                       "grouped asymmetric W4A8 prefill M=2048, K=2048, N=13312, G=128"),
 }
@@ -270,7 +275,12 @@ def time_oracle(w, seconds: float, openmp: bool = True):
     cores = os.cpu_count() if openmp else 1
     if w["regime"] == "prefill":
         w = dict(w, M=16, regime="prefill")
-    if w["kind"] == "w4a16":
+    if w["kind"] == "w4a16" and w["layout"] == 2:
+        x, wp, s = oracle_inputs(w)
+        blocks = o.blocks_b32(wp, s, w["K"])
+        call = lambda: o.linear_w4a16_b32_exact(x, blocks, w["K"])
+        what = "ref_linear_w4a16_b32_exact"
+    elif w["kind"] == "w4a16":
         x, wp, s = oracle_inputs(w)
         call = lambda: o.linear_w4a16_lanes(x, wp, s, w["K"], w["G"])
         what = "ref_linear_w4a16_lanes"
@@ -328,6 +338,8 @@ class Workload:
             x0, w0 = dev(x), dev(wp)
             if w["layout"] == 1:
                 w0 = ops.pack_interleaved_n64(w0, K)
+            elif w["layout"] == 2:
+                w0 = ops.pack_block32(w0, dev(s), K)
             self.x = [x0.clone() for _ in range(copies)]
             self.wt = [w0.clone() for _ in range(copies)]
             self.s = [dev(s) for _ in range(copies)]
@@ -383,7 +395,9 @@ class Workload:
     def kernel(self, i: int, flags: int = 1):
         w, ops = self.w, self.ops
         c = i % self.copies
-        if w["kind"] == "w4a16":
+        if w["kind"] == "w4a16" and w["layout"] == 2:
+            ops.linear_w4a16_b32(self.x[c], self.wt[c], K=w["K"], N=w["N"], flags=flags, out=self.y[c])
+        elif w["kind"] == "w4a16":
             ops.linear_w4a16_group(self.x[c], self.wt[c], self.s[c], w["G"], K=w["K"], N=w["N"],
                                    layout=w["layout"], flags=flags, out=self.y[c])
         elif w["kind"] == "w8a16":
@@ -470,9 +484,17 @@ def time_e2e(w, steps: int, chunk: int = 64):
         yd = torch.empty((M, N), dtype=torch.float32, device="cuda")
         yh = torch.empty((M, N), dtype=torch.float32).pin_memory()
 
+        if w["layout"] == 1:
+            wd = ops.pack_interleaved_n64(wd, K)
+        elif w["layout"] == 2:
+            wd = ops.pack_block32(wd, sd, K)
+
         def step():
             xd.copy_(xh, non_blocking=True)
-            ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, out=yd)
+            if w["layout"] == 2:
+                ops.linear_w4a16_b32(xd, wd, K=K, N=N, out=yd)
+            else:
+                ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, layout=w["layout"], out=yd)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 2
     elif w["kind"] == "w8a16":
@@ -494,6 +516,8 @@ def time_e2e(w, steps: int, chunk: int = 64):
         _, _, wp, s, z = synth.q4_group_inputs(1001, 1, N, K, G)
         xh = torch.from_numpy(synth.activations_f32(1001, M, K)).pin_memory()
         wd, sd, zd = torch.from_numpy(wp).cuda(), torch.from_numpy(s.view(np.int16)).cuda(), torch.from_numpy(z).cuda()
+        if w["layout"] == 1:
+            wd = ops.pack_interleaved_n64(wd, K)
         xd = torch.empty_like(xh, device="cuda")
         xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
         sx = torch.empty(M, dtype=torch.float32, device="cuda")
@@ -506,13 +530,15 @@ def time_e2e(w, steps: int, chunk: int = 64):
             xd.copy_(xh, non_blocking=True)
             st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
             assert st == 0
-            ops.linear_q4_group(xq, sx, wd, sd, zd, G, K=K, N=N, out=yd, workspace=ws)
+            ops.linear_q4_group(xq, sx, wd, sd, zd, G, K=K, N=N, layout=w["layout"], out=yd, workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
     else:
         x, W = synth.w4a8_inputs(1001, M, N, K)
         xh = torch.from_numpy(x).pin_memory()
         wq, sw = ops.quantize_matrix_q4(torch.from_numpy(W).cuda())
+        if w["layout"] == 1:
+            wq = ops.pack_interleaved_n64(wq, K)
         xd = torch.empty_like(xh, device="cuda")
         xq = torch.empty((M, K), dtype=torch.int8, device="cuda")
         sx = torch.empty(M, dtype=torch.float32, device="cuda")
@@ -525,7 +551,7 @@ def time_e2e(w, steps: int, chunk: int = 64):
             xd.copy_(xh, non_blocking=True)
             st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
             assert st == 0
-            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, out=yd, workspace=ws)
+            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, layout=w["layout"], out=yd, workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
     stream = torch.cuda.Stream()

@@ -60,8 +60,12 @@ typedef enum {
 /* Weight layouts accepted by the linears. */
 enum {
     W4_LAYOUT_ROWMAJOR = 0,  /* packed [N][ceil(K/2)] (int4) or [N][K] (int8) */
-    W4_LAYOUT_N64 = 1        /* int4 only: [N/64][K][32 B], byte d = channel d (low) | channel d+32 (high);
+    W4_LAYOUT_N64 = 1,       /* int4 only: [N/64][K][32 B], byte d = channel d (low) | channel d+32 (high);
                                 requires N % 64 == 0 (vllm-omni "The 4-bit CPU path": the block must tile N) */
+    W4_LAYOUT_B32 = 2        /* w4_linear_w4a16_group only, G = 32: inline-scale blocks ("Fused int4 ...",
+                                Going further: blocks of 32 with the scale beside the codes); row n is Kp/32
+                                blocks of 18 bytes, [f16 scale, little-endian][16 bytes: the signed nibbles of
+                                columns 32b .. 32b+31, low nibble = even column]; scales_f16 is not read */
 };
 
 /* Launch flags of the linears. */
@@ -292,6 +296,11 @@ size_t w4_chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32
  * permutation of nibbles (either encoding).  ESHAPE: N % 64 != 0. */
 w4_status w4_pack_interleaved_n64(const uint8_t *w_rowmajor, uint8_t *w_il, int64_t N, int64_t K,
                                   void *stream);
+
+/* pack_block32: W4A16 planes (packed signed nibbles [N][Kp/2], f16 scales
+ * [N][Kp/32]) -> the W4_LAYOUT_B32 blocks [N][Kp/32][18].  ESHAPE: Kp % 32. */
+w4_status w4_pack_block32(const uint8_t *w_rowmajor, const uint16_t *scales_f16, uint8_t *blocks, int64_t N,
+                          int64_t K, void *stream);
 
 /* ---- host queries ---------------------------------------------------------- */
 

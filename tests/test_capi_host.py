@@ -166,3 +166,14 @@ def test_linear_w8a16_validation(lib):
     assert f(1, 4, 4, x=None) == lib.W4_EINVAL
     assert lib.workspace_bytes(lib.OP_LINEAR_W8A16, 1, 2048, 2048) == 0
     assert lib.workspace_bytes(lib.OP_LINEAR_W8A16, 2048, 2048, 2048) == 2048 * 2048 * 2
+
+
+def test_block32_validation(lib):
+    r = lib.raw
+    f = lambda K, G, layout=2, s=None: r.w4_linear_w4a16_group(FAKE, FAKE, s, FAKE, 1, 8, K, G, layout, None, 0, 0, None)
+    assert f(64, 64) == lib.W4_ESHAPE          # blocks are groups of 32
+    assert f(64, 32, layout=3) == lib.W4_EINVAL
+    assert f(64, 32, layout=0) == lib.W4_EINVAL  # the plane layouts need the scales
+    assert r.w4_linear_q4(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 4, 2, None, 0, 0, None) == lib.W4_EINVAL
+    assert r.w4_pack_block32(FAKE, FAKE, FAKE, 4, 48, None) == lib.W4_ESHAPE
+    assert r.w4_pack_block32(FAKE, FAKE, FAKE, 0, 64, None) == lib.W4_OK

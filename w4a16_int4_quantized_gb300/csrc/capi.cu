@@ -172,13 +172,14 @@ w4_status w4_linear_w4a16_group(const uint16_t *x_bf16, const uint8_t *w, const 
                                 int64_t M, int64_t N, int64_t K, int64_t G, int32_t layout, void *workspace,
                                 size_t ws_bytes, uint32_t flags, void *stream) {
     if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
-    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64) return W4_EINVAL;
+    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64 && layout != W4_LAYOUT_B32) return W4_EINVAL;
     const int64_t Kp = K + (K & 1);
     if (G <= 0 || (G & 1) || (Kp % G) != 0) return W4_ESHAPE;
+    if (layout == W4_LAYOUT_B32 && G != 32) return W4_ESHAPE;
     if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
     if (layout == W4_LAYOUT_N64 && N % 64) return W4_ESHAPE;
     if (M == 0 || N == 0) return W4_OK;
-    if (!y || (K > 0 && (!x_bf16 || !w || !scales_f16))) return W4_EINVAL;
+    if (!y || (K > 0 && (!x_bf16 || !w || (layout != W4_LAYOUT_B32 && !scales_f16)))) return W4_EINVAL;
     const w4_status ws = check_workspace(W4_OP_LINEAR_W4A16, M, N, K, G, workspace, ws_bytes);
     if (ws != W4_OK) return ws;
     if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), as_stream(stream)));
@@ -270,6 +271,16 @@ w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, i
                                          as_stream(stream), &e);
     if (rc == W4_ECUDA) return cuda_status(e);
     return (w4_status)rc;
+}
+
+w4_status w4_pack_block32(const uint8_t *w_rowmajor, const uint16_t *scales_f16, uint8_t *blocks, int64_t N,
+                          int64_t K, void *stream) {
+    if (N < 0 || K < 0) return W4_EINVAL;
+    if ((K + (K & 1)) % 32) return W4_ESHAPE;
+    if (N >= kMaxDim || K >= kMaxDim) return W4_ESHAPE;
+    if (N == 0 || K == 0) return W4_OK;
+    if (!w_rowmajor || !scales_f16 || !blocks) return W4_EINVAL;
+    return cuda_status(w4::launch_pack_block32(w_rowmajor, scales_f16, blocks, N, K, as_stream(stream)));
 }
 
 size_t w4_chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32_t K0) {

@@ -596,6 +596,7 @@ int64_t kx_of(int64_t K) { return round_up(K, 8); }
 
 bool gemm_supported(const LinearArgs &a) {
     if (a.M <= 16) return false;
+    if (a.layout == W4_LAYOUT_B32) return false;  // inline-scale blocks: 16-row decode slices
     if (a.N > 0x7FFFFFFF || a.M > 0x7FFFFFFF) return false;
     if (reinterpret_cast<uintptr_t>(a.w) % 16) return false;
     if (a.kind == KIND_W4A8G && (a.layout != W4_LAYOUT_ROWMAJOR || a.G % 32)) return false;

@@ -74,6 +74,7 @@ struct GemvParams {
     int unit_k;      // columns per unit
     int unit_bytes;  // packed bytes per unit per row
     int wstride;     // shared row stride of the (row-major) weight tile (bytes)
+    int rawstride;   // inline-scale blocks: shared row stride of the raw block rows (bytes)
     int xstride;     // shared row stride of the activation tile (bytes)
     int sstride;     // shared row stride of the f32 scale tile (floats)
     int raw_off, w_off, x_off, sc_off, red_off;
@@ -532,8 +533,10 @@ W4_DEV void stage_unit_sums(const GemvParams &p, int k0, int nun, int nthr, uint
 // unit's partial (|sum| <= 32 * 127 * 128 < 2^24) is exact in the f32
 // accumulator and is converted to i32 before it is added, so the integer
 // result is exact for any K.
-template <int KIND, bool N64, int RB, int MT, int CPG>
+template <int KIND, int LAY, int RB, int MT, int CPG>
 __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvParams p) {
+    constexpr bool N64 = LAY == 1;  // interleaved [N/64][K][32] layout
+    constexpr bool B32 = LAY == 2;  // inline-scale blocks of 32
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wr = warp % p.WR, wk = warp / p.WR;
@@ -574,7 +577,8 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     }
     constexpr int kMaxSc = 2;
     uint4 sv[kMaxSc];
-    const bool svec = prefetch_scales<KIND>(p, row0, rows, u0, nun, nthr, sv, smem);
+    bool svec = false;
+    if constexpr (!B32) svec = prefetch_scales<KIND>(p, row0, rows, u0, nun, nthr, sv, smem);  // B32: scales in the blocks
     if constexpr (KIND == KIND_W4A8G) load_zero_points(p, row0, rows, u0, nun, nthr, smem);
 
     griddep_wait();  // x may be written, and y read, by the previous kernel
@@ -606,7 +610,10 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
             if (tid + i * nthr < lim) {
                 uint8_t *dst;
                 if constexpr (N64) dst = smem + p.raw_off + 16 * j;
-                else {
+                else if constexpr (B32) {  // raw block rows, repacked below
+                    const int r = fast_div(j, cpr_magic);
+                    dst = smem + p.raw_off + r * p.rawstride + 16 * (j - r * cpr);
+                } else {
                     const int r = fast_div(j, cpr_magic);
                     dst = smem + p.w_off + r * p.wstride + 16 * (j - r * cpr);
                 }
@@ -616,6 +623,22 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     }
     store_scales<KIND>(p, rows, nun, nthr, svec, sv, smem);
     __syncthreads();
+    if constexpr (B32) {
+        // blocks of 18 bytes -> the row-major code tile (16 bytes per block) and
+        // the f32 scale of each block; from here on the W4A16 G = 32 path
+        float *scf = reinterpret_cast<float *>(smem + p.sc_off);
+        const uint32_t nun_magic = div_magic((uint32_t)nun);
+        for (int i = tid; i < rows * nun; i += nthr) {
+            const int r = fast_div(i, nun_magic), b = i - r * nun;
+            const uint16_t *blk = reinterpret_cast<const uint16_t *>(smem + p.raw_off + r * p.rawstride + 18 * b);
+            uint32_t wd[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) wd[q] = (uint32_t)blk[1 + 2 * q] | ((uint32_t)blk[2 + 2 * q] << 16);
+            *reinterpret_cast<uint4 *>(smem + p.w_off + r * p.wstride + 16 * b) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            scf[r * p.sstride + b] = __half2float(__ushort_as_half(blk[0]));
+        }
+        __syncthreads();
+    }
     // Let the next kernel on the stream start (and begin its weight fetch)
     // once this CTA's tiles are in shared memory.
     griddep_launch_dependents();
@@ -892,8 +915,10 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
     const int64_t Kb = (p.K + 1) >> 1;
     for (int64_t o = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); o < total; o += warps) {
         const int64_t m = o / p.N, n = o - (o / p.N) * p.N;
+        const int64_t nb32 = (p.K + (p.K & 1) + 31) / 32;  // blocks per row (inline-scale layout)
         auto nibble = [&](int64_t k) -> unsigned {
             if (layout == 0) return (p.w[n * Kb + (k >> 1)] >> ((k & 1) * 4)) & 0xFu;
+            if (layout == 2) return (p.w[(n * nb32 + (k >> 5)) * 18 + 2 + ((k & 31) >> 1)] >> ((k & 1) * 4)) & 0xFu;
             const uint8_t b = p.w[((n >> 6) * p.K + k) * 32 + ((n & 63) & 31)];
             return ((n & 63) < 32) ? (b & 0xFu) : (b >> 4);
         };
@@ -948,7 +973,9 @@ __global__ void __launch_bounds__(256) generic_kernel(const __grid_constant__ Ge
                 }
 #pragma unroll
                 for (int s = 16; s; s >>= 1) part += __shfl_xor_sync(0xffffffffu, part, s);
-                out = fmaf(__half2float(__ushort_as_half(s16[n * p.ng + gi])), part, out);
+                const uint16_t sg = (layout == 2) ? (uint16_t)(p.w[(n * nb32 + gi) * 18] | (p.w[(n * nb32 + gi) * 18 + 1] << 8))
+                                                  : s16[n * p.ng + gi];
+                out = fmaf(__half2float(__ushort_as_half(sg)), part, out);
             }
             if (lane == 0) p.y[m * p.N + n] = out;
         }
@@ -961,12 +988,12 @@ struct Shape {
     int RB, WR, WK, S, MT;
 };
 
-template <int KIND, bool N64, int RB, int MT, int CPG>
+template <int KIND, int LAY, int RB, int MT, int CPG>
 cudaError_t launch_one(const GemvParams &p, int S, int threads, int smem, cudaStream_t st, bool pdl) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<KIND, N64, RB, MT, CPG>,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<KIND, LAY, RB, MT, CPG>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -991,7 +1018,7 @@ cudaError_t launch_one(const GemvParams &p, int S, int threads, int smem, cudaSt
     }
     cfg.attrs = attrs;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, N64, RB, MT, CPG>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<KIND, LAY, RB, MT, CPG>, p);
 }
 
 constexpr int kDirectWords = 16;  // words per row a thread holds (gemv_direct_kernel NW)
@@ -1039,22 +1066,22 @@ cudaError_t dispatch_direct(const GemvParams &p, const Shape &s, int threads, in
     return launch_direct<KIND, 16, 2, CPG>(p, s.S, threads, smem, st, pdl);
 }
 
-template <int KIND, bool N64, int CPG>
+template <int KIND, int LAY, int CPG>
 cudaError_t dispatch_rb_mt(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
     if (s.RB == 8) {
-        if (s.MT == 1) return launch_one<KIND, N64, 8, 1, CPG>(p, s.S, threads, smem, st, pdl);
-        return launch_one<KIND, N64, 8, 2, CPG>(p, s.S, threads, smem, st, pdl);
+        if (s.MT == 1) return launch_one<KIND, LAY, 8, 1, CPG>(p, s.S, threads, smem, st, pdl);
+        return launch_one<KIND, LAY, 8, 2, CPG>(p, s.S, threads, smem, st, pdl);
     }
-    if (s.MT == 1) return launch_one<KIND, N64, 16, 1, CPG>(p, s.S, threads, smem, st, pdl);
-    return launch_one<KIND, N64, 16, 2, CPG>(p, s.S, threads, smem, st, pdl);
+    if (s.MT == 1) return launch_one<KIND, LAY, 16, 1, CPG>(p, s.S, threads, smem, st, pdl);
+    return launch_one<KIND, LAY, 16, 2, CPG>(p, s.S, threads, smem, st, pdl);
 }
 
-template <int KIND, bool N64>
+template <int KIND, int LAY>
 cudaError_t dispatch_grouped(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
     switch (p.cpg) {
-        case 1: return dispatch_rb_mt<KIND, N64, 1>(p, s, threads, smem, st, pdl);
-        case 4: return dispatch_rb_mt<KIND, N64, 4>(p, s, threads, smem, st, pdl);
-        default: return dispatch_rb_mt<KIND, N64, 0>(p, s, threads, smem, st, pdl);
+        case 1: return dispatch_rb_mt<KIND, LAY, 1>(p, s, threads, smem, st, pdl);
+        case 4: return dispatch_rb_mt<KIND, LAY, 4>(p, s, threads, smem, st, pdl);
+        default: return dispatch_rb_mt<KIND, LAY, 0>(p, s, threads, smem, st, pdl);
     }
 }
 
@@ -1071,6 +1098,10 @@ bool geometry(const LinearArgs &a, GemvParams &p) {
     } else if (a.kind == KIND_W4A8) {
         if (Kp % 32) return false;
         p.cpg = 1; p.unit_k = 32; p.unit_bytes = 16; p.units = (int)(Kp / 32); p.ng = 0;
+    } else if (a.layout == W4_LAYOUT_B32) {  // inline-scale blocks: a unit is one 18-byte block
+        if (a.kind != KIND_W4A16 || a.G != 32 || Kp % 256) return false;  // rows of whole 16-byte chunks
+        p.cpg = 1; p.unit_k = 32; p.unit_bytes = 18; p.units = (int)(Kp / 32); p.ng = p.units;
+        p.Kb = 18 * p.units;
     } else {  // group-wise kinds: a unit is one group
         if (Kp % 32 || a.G % 32) return false;
         p.cpg = (int)(a.G / 32); p.unit_k = (int)a.G; p.unit_bytes = (int)(a.G / 2);
@@ -1090,12 +1121,15 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_ti
     const int span_k = p.upc * p.unit_k;
     const int tile_units = n64 ? p.upp : p.upc;
     const bool w8 = a.kind == KIND_W8A8 || a.kind == KIND_W8A16;
-    p.wstride = pad_to(tile_units * p.unit_bytes, w8 ? 32 : 16);
+    const bool b32 = a.layout == W4_LAYOUT_B32;
+    p.wstride = pad_to(tile_units * (b32 ? 16 : p.unit_bytes), w8 ? 32 : 16);  // b32: codes only
+    p.rawstride = (int)round_up((int64_t)p.upc * p.unit_bytes, 16);
     p.xstride = pad_to(span_k * 2, 64);  // staged as 16-bit pairs for every kind
     p.sstride = p.upc | 1;  // f32 scales per row, odd so the 8 rows of a warp hit 8 banks
     int off = 0;
     p.raw_off = off;
     if (n64) off += (int)round_up((int64_t)span_k * 32, 128);
+    if (b32) off += (int)round_up((int64_t)p.R * p.rawstride, 128);
     p.w_off = off;
     if (weight_tile) off += (int)round_up((int64_t)p.R * p.wstride, 128);
     p.x_off = off;
@@ -1122,6 +1156,7 @@ bool gemv_supported(const LinearArgs &a) {
     if (a.M > 16 || a.M < 1) return false;
     if (a.N > 0x3FFFFFFF || a.K > 0x7FFFFFF) return false;
     if ((a.kind == KIND_W8A8 || a.kind == KIND_W8A16) && a.layout != W4_LAYOUT_ROWMAJOR) return false;
+    if (a.layout == W4_LAYOUT_B32 && a.kind != KIND_W4A16) return false;
     GemvParams p = {};
     if (!geometry(a, p)) return false;
     if ((reinterpret_cast<uintptr_t>(a.w) % 16) != 0) return false;
@@ -1169,7 +1204,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
         for (;;) {
             q.upc = (int)round_up(ceil_div(p.units, S), ualign);
             S = (int)ceil_div(p.units, q.upc);  // no empty splits
-            worst.layout = W4_LAYOUT_N64;
+            worst.layout = (a.layout == W4_LAYOUT_B32) ? W4_LAYOUT_B32 : W4_LAYOUT_N64;
             const int a1 = plan_smem(worst, sw, q);
             worst.layout = W4_LAYOUT_ROWMAJOR;
             const int a2 = plan_smem(worst, sw, q);
@@ -1201,7 +1236,8 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     // from global memory, so shared memory holds only x and the scales and
     // more CTAs fit per SM (the same arithmetic, so the same bits).  For
     // M <= 8 the 128-bit staged tile streams HBM better.
-    if (!n64 && a.M > 8 && (a.kind == KIND_W4A16 || a.kind == KIND_W4A8) && (p.cpg == 1 || p.cpg == 2 || p.cpg == 4) &&
+    if (a.layout == W4_LAYOUT_ROWMAJOR && a.M > 8 && (a.kind == KIND_W4A16 || a.kind == KIND_W4A8) &&
+        (p.cpg == 1 || p.cpg == 2 || p.cpg == 4) &&
         (a.kind == KIND_W4A16 || p.cpg == 1)) {
         GemvParams q = p;
         const int dsmem = plan_smem(a, s, q, false);
@@ -1214,18 +1250,19 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     }
     switch (a.kind) {
         case KIND_W4A8:
-            return n64 ? dispatch_rb_mt<KIND_W4A8, true, 1>(p, s, threads, smem, st, pdl)
-                       : dispatch_rb_mt<KIND_W4A8, false, 1>(p, s, threads, smem, st, pdl);
+            return n64 ? dispatch_rb_mt<KIND_W4A8, 1, 1>(p, s, threads, smem, st, pdl)
+                       : dispatch_rb_mt<KIND_W4A8, 0, 1>(p, s, threads, smem, st, pdl);
         case KIND_W8A8:
-            return dispatch_rb_mt<KIND_W8A8, false, 1>(p, s, threads, smem, st, pdl);
+            return dispatch_rb_mt<KIND_W8A8, 0, 1>(p, s, threads, smem, st, pdl);
         case KIND_W8A16:
-            return dispatch_rb_mt<KIND_W8A16, false, 1>(p, s, threads, smem, st, pdl);
+            return dispatch_rb_mt<KIND_W8A16, 0, 1>(p, s, threads, smem, st, pdl);
         case KIND_W4A8G:
-            return n64 ? dispatch_grouped<KIND_W4A8G, true>(p, s, threads, smem, st, pdl)
-                       : dispatch_grouped<KIND_W4A8G, false>(p, s, threads, smem, st, pdl);
+            return n64 ? dispatch_grouped<KIND_W4A8G, 1>(p, s, threads, smem, st, pdl)
+                       : dispatch_grouped<KIND_W4A8G, 0>(p, s, threads, smem, st, pdl);
         default:
-            return n64 ? dispatch_grouped<KIND_W4A16, true>(p, s, threads, smem, st, pdl)
-                       : dispatch_grouped<KIND_W4A16, false>(p, s, threads, smem, st, pdl);
+            if (a.layout == W4_LAYOUT_B32) return dispatch_rb_mt<KIND_W4A16, 2, 1>(p, s, threads, smem, st, pdl);
+            return n64 ? dispatch_grouped<KIND_W4A16, 1>(p, s, threads, smem, st, pdl)
+                       : dispatch_grouped<KIND_W4A16, 0>(p, s, threads, smem, st, pdl);
     }
 }
 

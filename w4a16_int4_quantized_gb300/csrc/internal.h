@@ -43,6 +43,8 @@ cudaError_t launch_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint
                                       cudaStream_t st);
 cudaError_t launch_dot_i32_q4(const int8_t *xq, const uint8_t *wrow, int64_t K, int32_t *out, cudaStream_t st);
 cudaError_t launch_pack_n64(const uint8_t *w, uint8_t *il, int64_t N, int64_t K, cudaStream_t st);
+cudaError_t launch_pack_block32(const uint8_t *w, const uint16_t *s, uint8_t *blocks, int64_t N, int64_t K,
+                                cudaStream_t st);
 
 // gemv.cu -- small-M tensor-core GEMV (M <= 16) and the generic fallback.
 bool gemv_supported(const LinearArgs &a);

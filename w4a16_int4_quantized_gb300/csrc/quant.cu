@@ -177,4 +177,30 @@ cudaError_t launch_pack_n64(const uint8_t *w, uint8_t *il, int64_t N, int64_t K,
     return cudaGetLastError();
 }
 
+// pack_block32: one thread per 18-byte block: the f16 scale, then the
+// block's 16 code bytes (W4A16 planes -> inline-scale blocks of 32).
+__global__ void pack_block32_kernel(const uint8_t *__restrict__ w, const uint16_t *__restrict__ s,
+                                    uint8_t *__restrict__ blocks, int64_t N, int64_t nb) {
+    const int64_t total = N * nb;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / nb, b = i - n * nb;
+        uint8_t *blk = blocks + i * 18;
+        const uint16_t sc = s[i];
+        blk[0] = (uint8_t)(sc & 0xFF);
+        blk[1] = (uint8_t)(sc >> 8);
+        const uint8_t *src = w + n * (nb * 16) + 16 * b;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) blk[2 + j] = src[j];
+    }
+}
+
+cudaError_t launch_pack_block32(const uint8_t *w, const uint16_t *s, uint8_t *blocks, int64_t N, int64_t K,
+                                cudaStream_t st) {
+    const int64_t nb = (K + (K & 1)) / 32;
+    const int64_t total = N * nb;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>((total + 255) / 256, 152 * 16));
+    pack_block32_kernel<<<(unsigned)grid, 256, 0, st>>>(w, s, blocks, N, nb);
+    return cudaGetLastError();
+}
+
 }  // namespace w4

@@ -20,7 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libw4gb300.so")
 
 W4_OK, W4_EINVAL, W4_ESHAPE, W4_ECUDA = 0, 1, 2, 3
-LAYOUT_ROWMAJOR, LAYOUT_N64 = 0, 1
+LAYOUT_ROWMAJOR, LAYOUT_N64, LAYOUT_B32 = 0, 1, 2
 FLAG_PDL = 1
 OP_LINEAR_Q4, OP_LINEAR_Q8, OP_LINEAR_W4A16, OP_LINEAR_Q4_GROUP, OP_LINEAR_W8A16 = 0, 1, 2, 3, 4
 CHAIN_MAX_LINEARS, CHAIN_MAX_K = 64, 8192
@@ -48,6 +48,7 @@ SIGNATURES = [
     ("w4_chain_q4", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
     ("w4_chain_workspace_bytes", _sz, [_vp, _i32, _i32]),
     ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
+    ("w4_pack_block32", _i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
     ("w4_workspace_bytes", _sz, [_i32, _i64, _i64, _i64, _i64]),
     ("w4_device_status", _i32, [_vp, _i32]),
     ("w4_last_cuda_error", _i32, []),
@@ -272,6 +273,28 @@ def pack_interleaved_n64(w: torch.Tensor, K: int, stream=None) -> torch.Tensor:
     il = torch.empty((N // 64, K, 32), dtype=torch.uint8, device=w.device)
     _check(raw.w4_pack_interleaved_n64(_ptr(w), _ptr(il), N, K, _stream(stream)), "w4_pack_interleaved_n64")
     return il
+
+
+def linear_w4a16_b32(x, blocks, K: int | None = None, N: int | None = None, flags: int = 0, out=None,
+                     stream=None) -> torch.Tensor:
+    """Group-wise W4A16 (G = 32) reading inline-scale blocks [N][Kp/32 * 18]."""
+    assert x.element_size() == 2
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    N = blocks.shape[0] if N is None else N
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _check(raw.w4_linear_w4a16_group(_ptr(x), _ptr(blocks), None, _ptr(y), M, N, K, 32, LAYOUT_B32, None, 0, flags,
+                                     _stream(stream)), "w4_linear_w4a16_group")
+    return y
+
+
+def pack_block32(w: torch.Tensor, scales: torch.Tensor, K: int, stream=None) -> torch.Tensor:
+    """W4A16 planes (packed [N][Kp/2], f16 scales [N][Kp/32]) -> inline-scale blocks [N][Kp/32 * 18]."""
+    N = w.shape[0]
+    nb = (K + (K & 1)) // 32
+    out = torch.empty((N, nb * 18), dtype=torch.uint8, device=w.device)
+    _check(raw.w4_pack_block32(_ptr(w), _ptr(scales), _ptr(out), N, K, _stream(stream)), "w4_pack_block32")
+    return out
 
 
 def workspace_bytes(op: int, M: int, N: int, K: int, G: int = 0) -> int:
