@@ -416,7 +416,9 @@ class Workload:
             st = self.ops.raw.w4_quantize_row_q8(self.xf[c].data_ptr(), M, K, self.x[c].data_ptr(),
                                                   self.sx[c].data_ptr(), None, self.ops._stream())
             assert st == 0
-            self.kernel(i, flags=0)  # the quantizer writes x: no early start
+            # the linear reads x only after griddepcontrol.wait (the quantizer
+            # has finished); before it, only its weight fetch overlaps
+            self.kernel(i, flags)
         else:
             self.kernel(i, flags)
 
@@ -492,9 +494,9 @@ def time_e2e(w, steps: int, chunk: int = 64):
         def step():
             xd.copy_(xh, non_blocking=True)
             if w["layout"] == 2:
-                ops.linear_w4a16_b32(xd, wd, K=K, N=N, out=yd)
+                ops.linear_w4a16_b32(xd, wd, K=K, N=N, flags=ops.FLAG_PDL, out=yd)
             else:
-                ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, layout=w["layout"], out=yd)
+                ops.linear_w4a16_group(xd, wd, sd, G, K=K, N=N, layout=w["layout"], flags=ops.FLAG_PDL, out=yd)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 2
     elif w["kind"] == "w8a16":
@@ -509,7 +511,7 @@ def time_e2e(w, steps: int, chunk: int = 64):
 
         def step():
             xd.copy_(xh, non_blocking=True)
-            ops.linear_w8a16(xd, wd, sd, out=yd, workspace=ws)
+            ops.linear_w8a16(xd, wd, sd, flags=ops.FLAG_PDL, out=yd, workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
     elif w["kind"] == "w4a8g":
@@ -530,7 +532,7 @@ def time_e2e(w, steps: int, chunk: int = 64):
             xd.copy_(xh, non_blocking=True)
             st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
             assert st == 0
-            ops.linear_q4_group(xq, sx, wd, sd, zd, G, K=K, N=N, layout=w["layout"], out=yd, workspace=ws)
+            ops.linear_q4_group(xq, sx, wd, sd, zd, G, K=K, N=N, layout=w["layout"], flags=ops.FLAG_PDL, out=yd, workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
     else:
@@ -551,7 +553,7 @@ def time_e2e(w, steps: int, chunk: int = 64):
             xd.copy_(xh, non_blocking=True)
             st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
             assert st == 0
-            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, layout=w["layout"], out=yd, workspace=ws)
+            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, layout=w["layout"], flags=ops.FLAG_PDL, out=yd, workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
     stream = torch.cuda.Stream()

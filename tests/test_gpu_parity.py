@@ -116,7 +116,7 @@ def w4a8_case(ora, seed, M, N, K):
     return xq, sx, w, sw
 
 
-LIN_SHAPES = [(2048, 2048), (37, 200), (64, 2047), (3072, 2048), (1024, 3072), (100, 64), (1, 32)]
+LIN_SHAPES = [(2048, 2048), (37, 200), (64, 2047), (3072, 2048), (1024, 3072), (100, 64), (1, 32), (1024, 32)]
 
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 9, 16])
@@ -202,7 +202,8 @@ def w4a16_check(y, ora, x, w, s, K, G):
 
 @pytest.mark.parametrize("M", [1, 2, 4, 8, 9, 16])
 @pytest.mark.parametrize("N,K,G", [(2048, 2048, 32), (2048, 2047, 32), (3072, 2048, 128), (64, 384, 64),
-                                   (37, 384, 32), (100, 1024, 256), (64, 2048, 2048)])
+                                   (37, 384, 32), (100, 1024, 256), (64, 2048, 2048),
+                                   (1024, 1024, 128), (1024, 32, 32), (1088, 1024, 128)])
 def test_linear_w4a16(ops, ora, M, N, K, G):
     x, w, s = synth.w4a16_inputs(91 + N + K + G, M, N, K, G)
     y = host(ops.linear_w4a16_group(dev(x), dev(w), dev(s), G, K=K))
@@ -242,6 +243,37 @@ def test_w4a16_batch_invariance(ops, N, K, G):
     for m in range(M):
         y1 = host(ops.linear_w4a16_group(dev(x[m:m + 1]), wd, sd, G, K=K))
         assert np.array_equal(bits(y1[0]), bits(yb[m])), m
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("N,K,G", [(2048, 2048, 32), (2048, 2047, 32), (13312, 2048, 128), (1024, 1024, 128),
+                                   (3072, 2048, 128), (4096, 8192, 128), (1000, 4096, 32)])
+def test_w4a16_pdl_same_bits(ops, ora, M, N, K, G):
+    """With W4_FLAG_PDL, large-N decode calls stream whole-SM row ranges with
+    bulk copies (a different kernel); the arithmetic, and so every bit, is the
+    one of the call without the flag.  Sampled rows against the oracle."""
+    x, w, s = synth.w4a16_inputs(131 + M + N + K, M, N, K, G)
+    xd, wd, sd = dev(x), dev(w), dev(s)
+    y0 = host(ops.linear_w4a16_group(xd, wd, sd, G, K=K))
+    y1 = host(ops.linear_w4a16_group(xd, wd, sd, G, K=K, flags=ops.FLAG_PDL))
+    assert np.array_equal(bits(y1), bits(y0))
+    rows = np.sort(np.random.default_rng(N + M).choice(N, min(N, 192), replace=False))
+    w4a16_check(np.ascontiguousarray(y1[:, rows]), ora, x, w[rows], s[rows], K, G)
+    assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("N,K", [(2048, 2048), (13312, 2048)])
+def test_linear_q4_pdl_bitexact(ops, ora, M, N, K):
+    """The PDL-launched row quantizer followed by a PDL linear: the oracle's bits."""
+    x = synth.activations_f32(141 + M, M, K)
+    W = synth.weights_f32(142 + N, N, K)
+    wq, sw = ora.quantize_matrix_q4(W)
+    xq_d, sx_d, _ = ops.quantize_row_q8(dev(x))
+    y = host(ops.linear_q4(xq_d, sx_d, dev(wq), dev(sw), K=K, flags=ops.FLAG_PDL))
+    xq, sx, _ = ora.quantize_row_q8(x)
+    assert np.array_equal(host(xq_d), xq) and np.array_equal(bits(host(sx_d)), bits(sx))
+    assert np.array_equal(bits(y), bits(ora.linear_q4(xq, sx, wq, sw, K)))
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])

@@ -77,7 +77,7 @@ struct GemvParams {
     int rawstride;   // inline-scale blocks: shared row stride of the raw block rows (bytes)
     int xstride;     // shared row stride of the activation tile (bytes)
     int sstride;     // shared row stride of the f32 scale tile (floats)
-    int raw_off, w_off, x_off, sc_off, red_off;
+    int raw_off, w_off, x_off, sc_off, red_off, bar_off;
     int zc_off, xs_off;  // W4A8G: (8 - z) per [row][unit] (int), activation sums per [m][unit] (int)
     int x_vec;       // activation rows can be read with aligned vector loads
     int s_vec;       // scale rows can be read as 16-byte vectors
@@ -161,8 +161,10 @@ W4_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32
 
 // Division by a CTA-invariant divisor d (< 2^16) of j < 2^16: floor(j / d)
 // = umulhi(j, ceil(2^32 / d)).
+// j / d for 0 <= j < 2^32 / d by one high multiply with ceil(2^32 / d); for
+// d = 1 the multiplier (2^32) does not fit and is stored as 0, meaning j / 1.
 W4_DEV uint32_t div_magic(uint32_t d) { return 0xFFFFFFFFu / d + 1u; }
-W4_DEV int fast_div(int j, uint32_t magic) { return (int)__umulhi((uint32_t)j, magic); }
+W4_DEV int fast_div(int j, uint32_t magic) { return magic ? (int)__umulhi((uint32_t)j, magic) : j; }
 
 // One unit (CPG chunks of 32 columns) of one warp: MMA partial sums for the
 // warp's 16-row block (rows g, g + 8 of each thread) against MT 8-row
@@ -903,6 +905,170 @@ __global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant_
     combine_and_store<KIND, RB, MT>(p, acc, wr, wk, lane, g, t, row0 + rbase, smem);
 }
 
+// ---------------------------------------------------------------- streaming kernel
+//
+// gemv_kernel's arithmetic on the row-major layout for large N and M <= 8,
+// with the data movement rebuilt around whole-SM row ranges:
+//  * each CTA owns ~N / 152 consecutive rows (a whole number of 8-row
+//    blocks) over the full K range;
+//  * its entire weight range is requested at once, one bulk async copy per
+//    row into a padded shared row, each 8-row block completing on its own
+//    mbarrier -- all before the PDL wait, and with the PDL trigger at entry:
+//    a CTA takes under half of an SM's shared memory, so the next launch's
+//    CTA shares the SM and fetches its whole range while this one computes,
+//    and no third launch can start before this one ends;
+//  * warps walk their row blocks in order as the blocks land, and the K-split
+//    warps are combined once at the end.
+// The K split (WK warps, one split per row), the unit -> warp assignment, the
+// MMA operand order, the fold and the combine order are gemv_kernel's, so the
+// results are bit-identical to it (and so across M and layouts).
+template <int KIND, int RB, int CPG, int NRBW>
+__global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
+    static_assert(KIND == KIND_W4A16 || KIND == KIND_W4A8, "row-major int4 kinds");
+    griddep_launch_dependents();
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr bool kInt = kIntAcc<KIND>;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int wr = warp % p.WR, wk = warp / p.WR;
+    const int g = lane >> 2, t = lane & 3;
+    const int row0 = blockIdx.x * p.R;
+    const int rows = min(p.R, p.N - row0);
+    const int nrb = (rows + RB - 1) / RB;
+    const int nun = p.units;
+    const int nthr = blockDim.x;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+
+    // ---- 1. the whole weight range in flight (no earlier kernel writes weights).
+    if (tid == 0) {
+        for (int b = 0; b < nrb; ++b) mbar_init(&bars[b], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            for (int b = 0; b < nrb; ++b) mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(RB, rows - b * RB) * p.Kb));
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb, &bars[r / RB]);
+    }
+    uint4 sv[2];
+    const bool svec = prefetch_scales<KIND>(p, row0, rows, 0, nun, nthr, sv, smem);
+
+    griddep_wait();  // x may be written, and y read, by the previous kernel
+    stage_x<KIND>(p, 0, nun * p.unit_k, nthr, smem);
+    store_scales<KIND>(p, rows, nun, nthr, svec, sv, smem);
+    __syncthreads();
+
+    // ---- 2. the warp's row blocks, in order, as they land.
+    using Acc = typename std::conditional<kInt, int, float>::type;
+    Acc acc[NRBW][4];
+#pragma unroll
+    for (int j = 0; j < NRBW; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[j][i] = 0;
+    const bool xvalid[1] = {g < p.M};
+    const uint8_t *xrow = smem + p.x_off + (xvalid[0] ? g : 0) * p.xstride + 16 * t;
+    const float *scf = reinterpret_cast<const float *>(smem + p.sc_off);
+    const int WK = p.WK;
+    const int cpg = CPG > 0 ? CPG : p.cpg;
+    bool ok = true;
+#pragma unroll
+    for (int j = 0; j < NRBW; ++j) {
+        const int rb = wr + j * p.WR;
+        if (rb >= nrb) break;
+        if (!mbar_wait_bounded(&bars[rb], 0)) {
+            ok = false;
+            continue;
+        }
+        const uint8_t *wrow = smem + p.w_off + (rb * RB + g) * p.wstride;
+        const uint8_t *wrow8 = wrow + 8 * p.wstride;
+        const float *sc0 = scf + (rb * RB + g) * p.sstride;
+        const float *sc1 = scf + (rb * RB + g + 8) * p.sstride;
+        auto fold = [&](const float (&part)[1][4], int u) {
+            if constexpr (KIND == KIND_W4A16) {
+                const float s0 = sc0[u];
+                const float s1 = (RB == 16) ? sc1[u] : 0.0f;
+                acc[j][0] = fmaf(s0, part[0][0], acc[j][0]);
+                acc[j][1] = fmaf(s0, part[0][1], acc[j][1]);
+                acc[j][2] = fmaf(s1, part[0][2], acc[j][2]);
+                acc[j][3] = fmaf(s1, part[0][3], acc[j][3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) acc[j][i] += __float2int_rn(part[0][i]);
+            }
+        };
+        auto run_unit = [&](int u, float (&part)[1][4]) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) part[0][i] = 0.0f;
+            const uint8_t *xr[1] = {xrow + 64 * cpg * u};
+            unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, part);
+        };
+        int u = wk;
+        for (; u + 3 * WK < nun; u += 4 * WK) {
+            float part[4][1][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) run_unit(u + q * WK, part[q]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) fold(part[q], u + q * WK);
+        }
+        for (; u < nun; u += WK) {
+            float part[1][4];
+            run_unit(u, part);
+            fold(part, u);
+        }
+    }
+    if (!ok) {
+        if (lane == 0 && p.status) atomicOr(p.status, kStatusCopyTimeout);
+        // give copies still in flight one more bounded wait before the CTA's shared memory goes away
+        for (int b = wr; b < nrb; b += p.WR) (void)mbar_wait_bounded(&bars[b], 0);
+    }
+
+    // ---- 3. combine the K-split warps in index order, then the epilogue.
+    uint32_t *red = reinterpret_cast<uint32_t *>(smem + p.red_off);
+    if (WK > 1) {
+        __syncthreads();  // red may alias the weight tile
+        if (wk > 0) {
+#pragma unroll
+            for (int j = 0; j < NRBW; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    red[((((wk - 1) * p.WR + wr) * NRBW + j) * 32 + lane) * 4 + i] =
+                        kInt ? (uint32_t)acc[j][i] : __float_as_uint((float)acc[j][i]);
+        }
+        __syncthreads();
+        if (wk != 0) return;
+        for (int w2 = 1; w2 < WK; ++w2)
+#pragma unroll
+            for (int j = 0; j < NRBW; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t v = red[((((w2 - 1) * p.WR + wr) * NRBW + j) * 32 + lane) * 4 + i];
+                    if constexpr (kInt) acc[j][i] += (int)v;
+                    else acc[j][i] += __uint_as_float(v);
+                }
+    }
+#pragma unroll
+    for (int j = 0; j < NRBW; ++j) {
+        const int rb = wr + j * p.WR;
+        if (rb >= nrb) break;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (RB == 8 && i >= 2) continue;
+            const int m = 2 * t + (i & 1);
+            const int n = row0 + rb * RB + g + 8 * (i >> 1);
+            if (m >= p.M || n >= p.N) continue;
+            float out;
+            if constexpr (kInt) {
+                const float sw = static_cast<const float *>(p.scale)[n];
+                out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[j][i]), p.sx[m]), sw);
+            } else {
+                out = acc[j][i];
+            }
+            p.y[(size_t)m * p.N + n] = out;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- generic fallback
 
 // One warp per output element; any shape, any layout.  Integer kinds are
@@ -1056,6 +1222,44 @@ cudaError_t launch_direct(const GemvParams &p, int S, int threads, int smem, cud
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int KIND, int RB, int CPG, int NRBW>
+cudaError_t launch_stream(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    auto *kern = gemv_stream_kernel<KIND, RB, CPG, NRBW>;
+    std::call_once(once, [kern] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(p.N, p.R), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int KIND, int RB, int CPG>
+cudaError_t dispatch_stream_nrbw(const GemvParams &p, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
+    switch (nrbw) {
+        case 1: return launch_stream<KIND, RB, CPG, 1>(p, threads, smem, st, pdl);
+        case 2: return launch_stream<KIND, RB, CPG, 2>(p, threads, smem, st, pdl);
+        case 3: return launch_stream<KIND, RB, CPG, 3>(p, threads, smem, st, pdl);
+        default: return launch_stream<KIND, RB, CPG, 4>(p, threads, smem, st, pdl);
+    }
+}
+
+template <int KIND, int CPG>
+cudaError_t dispatch_stream(const GemvParams &p, int rb, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
+    if (rb == 16) return dispatch_stream_nrbw<KIND, 16, CPG>(p, nrbw, threads, smem, st, pdl);
+    return dispatch_stream_nrbw<KIND, 8, CPG>(p, nrbw, threads, smem, st, pdl);
+}
+
 template <int KIND, int CPG>
 cudaError_t dispatch_direct(const GemvParams &p, const Shape &s, int threads, int smem, cudaStream_t st, bool pdl) {
     if (s.RB == 8) {
@@ -1150,6 +1354,63 @@ int plan_smem(const LinearArgs &a, const Shape &s, GemvParams &p, bool weight_ti
     return off;
 }
 
+constexpr int kStreamSmemPerCta = 112 * 1024;  // two CTAs (and their reserved 1 KB each) per SM
+constexpr int kStreamMaxBlocks = 16;            // row blocks per CTA (4 warps along rows x NRBW <= 4)
+constexpr int kStreamMinSmem = 80 * 1024;               // dynamic shared memory requested at least
+
+// Plans the streaming kernel for a call; false when it does not apply.
+// p must hold the call's geometry, upc = units (no K split) and WK.
+bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out, int &threads, int &smem) {
+    if (a.layout != W4_LAYOUT_ROWMAJOR || a.M > 8 || (a.kind != KIND_W4A16 && a.kind != KIND_W4A8)) return false;
+    if (p.Kb % 16 != 0 || p.upc != p.units) return false;
+    const int span_k = p.units * p.unit_k;
+    p.wstride = pad_to(p.Kb, 16);
+    p.xstride = pad_to(span_k * 2, 64);
+    p.sstride = p.upc | 1;
+    const int xbytes = (int)round_up((int64_t)a.M * p.xstride, 128);
+    const int per_row = p.wstride + (a.kind == KIND_W4A16 ? 4 * p.sstride : 0);
+    const int fixed = 128 + xbytes + 2 * 128;
+    // rows per CTA: the fewest waves of 152 CTAs, rows spread evenly, a whole number of RB-row blocks
+    auto rows_for = [&](int RB) -> int {
+        const int rmax = std::min((kStreamSmemPerCta - fixed) / per_row / RB * RB, kStreamMaxBlocks * RB);
+        if (rmax < RB) return 0;
+        const int64_t waves = ceil_div(a.N, (int64_t)152 * rmax);
+        return (int)std::min<int64_t>(rmax, round_up(ceil_div(a.N, 152 * waves), RB));
+    };
+    const int R8 = rows_for(8), R16 = rows_for(16);
+    if (R8 == 0) return false;
+    const int RB = (R16 > 0 && R16 * 100 <= R8 * 103) ? 16 : 8;
+    const int R = RB == 16 ? R16 : R8;
+    const int nrb = R / RB;
+    const int WR = std::min(4, nrb);
+    const int nrbw = (int)ceil_div(nrb, WR);
+    if (nrbw > 4) return false;
+    p.R = R;
+    p.WR = WR;
+    int off = 0;
+    p.bar_off = off;
+    off += (int)round_up((int64_t)nrb * 8, 128);
+    p.w_off = off;
+    off += (int)round_up((int64_t)R * p.wstride, 128);
+    p.x_off = off;
+    off += xbytes;
+    p.sc_off = off;
+    if (a.kind == KIND_W4A16) off += (int)round_up((int64_t)R * p.sstride * 4, 128);
+    // the K-split combine reuses the weight tile once every warp is done with it
+    const int red = (p.WK - 1) * WR * nrbw * 32 * 16;
+    p.red_off = p.w_off;
+    if (red > R * p.wstride) {
+        p.red_off = off;
+        off += red;
+    }
+    if (off > kStreamSmemPerCta) return false;
+    rb_out = RB;
+    nrbw_out = nrbw;
+    threads = 32 * WR * p.WK;
+    smem = std::max(off, kStreamMinSmem);
+    return true;
+}
+
 }  // namespace
 
 bool gemv_supported(const LinearArgs &a) {
@@ -1232,6 +1493,21 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     s.S = S;
     const int threads = 32 * p.WR * p.WK;
     const bool pdl = (a.flags & W4_FLAG_PDL) != 0;
+    // Large N, M <= 8, no K split, PDL: the streaming kernel (same arithmetic).
+    // Without PDL its per-row bulk copies have nothing to overlap with, and
+    // the staged kernel's register loads reach HBM sooner.
+    {
+        GemvParams q = p;
+        int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
+        if (pdl && a.kind == KIND_W4A16 && S == 1 && plan_stream(a, q, rb, nrbw, sthreads, ssmem) &&
+            ceil_div(a.N, (int64_t)q.R) >= 120) {
+            switch (p.cpg) {
+                case 1: return dispatch_stream<KIND_W4A16, 1>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+                case 4: return dispatch_stream<KIND_W4A16, 4>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+                default: return dispatch_stream<KIND_W4A16, 0>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+            }
+        }
+    }
     // Row-major int4 with two activation tiles (M > 8): fragments straight
     // from global memory, so shared memory holds only x and the scales and
     // more CTAs fit per SM (the same arithmetic, so the same bits).  For

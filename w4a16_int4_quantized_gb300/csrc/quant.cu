@@ -61,11 +61,17 @@ W4_DEV int quant_code(float v, float s, int Q) {
 }
 
 // One CTA per row: max|v|, the scale, the codes, and (optionally) their sum.
+// Launched with programmatic stream serialization: it touches memory only
+// after griddepcontrol.wait (the previous kernel may write x or read q), and
+// lets the next kernel start at once, so a linear after it fetches its
+// weights while the rows are quantised.
 __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *__restrict__ x, int64_t K, int Q,
                                                                  int8_t *__restrict__ q, float *__restrict__ s,
                                                                  int32_t *__restrict__ rowsum) {
     __shared__ float redf[32];
     __shared__ int redi[32];
+    griddep_launch_dependents();
+    griddep_wait();
     const int64_t row = blockIdx.x;
     const float *xr = x + row * K;
     float amax = 0.0f;
@@ -154,8 +160,16 @@ __global__ void pack_n64_kernel(const uint8_t *__restrict__ w, uint8_t *__restri
 cudaError_t launch_quantize_rows(const float *x, int64_t rows, int64_t K, int Q, int8_t *q, float *s,
                                  int32_t *rowsum, cudaStream_t st) {
     if (rows > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    quantize_rows_kernel<<<(unsigned)rows, kThreads, 0, st>>>(x, K, Q, q, s, rowsum);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_rows_kernel, x, K, Q, q, s, rowsum);
 }
 
 cudaError_t launch_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw,
