@@ -386,10 +386,13 @@ class Workload:
 
     @property
     def launches_per_step(self) -> int:
-        if self.w["kind"] == "w4a16":
+        w = self.w
+        if w["kind"] == "w4a16":
             return 1
-        if self.w["kind"] == "w8a16":
+        if w["kind"] == "w8a16":
             return 1 + (1 if self.ws is not None else 0)  # (f32 -> bf16 prepass), linear
+        if w["kind"] == "w4a8" and w["M"] <= 8 and w["layout"] == 0 and w["N"] >= 1024:
+            return 1  # the rows are quantised inside the linear
         return 2 + (1 if self.ws is not None else 0)  # quantize, (int8 -> f16 prepass), linear
 
     def kernel(self, i: int, flags: int = 1):
@@ -405,12 +408,20 @@ class Workload:
         elif w["kind"] == "w4a8g":
             ops.linear_q4_group(self.x[c], self.sx[c], self.wt[c], self.s[c], self.z[c], w["G"], K=w["K"],
                                 N=w["N"], layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
+        elif self.launches_per_step == 1:  # W4A8 whose rows are quantised inside the linear: that one kernel
+            self.step(i, flags)
         else:
             ops.linear_q4(self.x[c], self.sx[c], self.wt[c], self.s[c], K=w["K"], N=w["N"],
                           layout=w["layout"], flags=flags, out=self.y[c], workspace=self.ws)
 
     def step(self, i: int, flags: int = 1):
-        if self.w["kind"] not in ("w4a16", "w8a16"):
+        w = self.w
+        if w["kind"] == "w4a8":
+            # quantize_row_q8 + linear_q4 as one library call (fused for M <= 8)
+            c = i % self.copies
+            self.ops.linear_q4_f32(self.xf[c], self.wt[c], self.s[c], K=w["K"], N=w["N"], layout=w["layout"],
+                                   flags=flags, out=self.y[c], xq=self.x[c], sx=self.sx[c], workspace=self.ws)
+        elif w["kind"] not in ("w4a16", "w8a16"):
             c = i % self.copies
             M, K = self.xf[c].shape
             st = self.ops.raw.w4_quantize_row_q8(self.xf[c].data_ptr(), M, K, self.x[c].data_ptr(),
@@ -551,9 +562,8 @@ def time_e2e(w, steps: int, chunk: int = 64):
 
         def step():
             xd.copy_(xh, non_blocking=True)
-            st = ops.raw.w4_quantize_row_q8(xd.data_ptr(), M, K, xq.data_ptr(), sx.data_ptr(), None, ops._stream())
-            assert st == 0
-            ops.linear_q4(xq, sx, wq, sw, K=K, N=N, layout=w["layout"], flags=ops.FLAG_PDL, out=yd, workspace=ws)
+            ops.linear_q4_f32(xd, wq, sw, K=K, N=N, layout=w["layout"], flags=ops.FLAG_PDL, out=yd, xq=xq, sx=sx,
+                              workspace=ws)
             yh.copy_(yd, non_blocking=True)
         h2d = xh.numel() * 4
     stream = torch.cuda.Stream()
@@ -1098,7 +1108,8 @@ def run_ours(args, world, rank, local):
                    "G": w["G"], "parallelism": "replicas" if world > 1 else "single",
                    "l2": f"inputs larger than L2: {copies} rotating input copies "
                          f"({copies * weight_bytes(w) / 2**20:.0f} MiB of weights) vs L2 {l2 / 2**20:.0f} MiB",
-                   "step": {"w4a8": "quantize_row_q8 + linear_q4", "w4a8g": "quantize_row_q8 + linear_q4_group",
+                   "step": {"w4a8": "linear_q4_f32 (quantize_row_q8 + linear_q4 in one call)",
+                            "w4a8g": "quantize_row_q8 + linear_q4_group",
                             "w8a16": "linear_w8a16"}.get(
                        w["kind"], "linear_w4a16_group"),
                    "timing": "CUDA events around CUDA-graph replays of exactly `steps` steps"},

@@ -143,6 +143,19 @@ w4_status w4_linear_q4(const int8_t *xq, const float *sx, const uint8_t *w, cons
                        float *y, int64_t M, int64_t N, int64_t K, int32_t layout,
                        void *workspace, size_t ws_bytes, uint32_t flags, void *stream);
 
+/* quantize_row_q8 followed by linear_q4, as one call (docs.rs
+ * ftts_kernels::int4 and ::int8: activations are quantised per row before
+ * the W4A8 linear).  x [M][K] f32 device; xq [M][K] int8 and sx [M] f32
+ * receive exactly what w4_quantize_row_q8 writes; y [M][N] what
+ * w4_linear_q4 writes for them -- bit for bit.  For M <= 8 on the row-major
+ * layout with N >= 1024 the quantisation runs inside the linear (every
+ * thread block quantises the rows it needs; one launch); otherwise the two
+ * kernels run in order.  Other arguments, limits and errors: those of
+ * w4_linear_q4 and w4_quantize_row_q8. */
+w4_status w4_linear_q4_f32(const float *x, const uint8_t *w, const float *sw, float *y, int8_t *xq, float *sx,
+                           int64_t M, int64_t N, int64_t K, int32_t layout, void *workspace, size_t ws_bytes,
+                           uint32_t flags, void *stream);
+
 /* linear_q8, W8A8 (docs.rs ftts_kernels::int8, linear_q8): the same
  * epilogue over acc[m][n] = sum_k xq[m][k] * w[n][k] (exact i32), w [N][K]
  * int8 (from w4_quantize_matrix_q8), sw [N].  Bit-exact with the oracle.

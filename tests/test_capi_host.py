@@ -177,3 +177,16 @@ def test_block32_validation(lib):
     assert r.w4_linear_q4(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 4, 4, 2, None, 0, 0, None) == lib.W4_EINVAL
     assert r.w4_pack_block32(FAKE, FAKE, FAKE, 4, 48, None) == lib.W4_ESHAPE
     assert r.w4_pack_block32(FAKE, FAKE, FAKE, 0, 64, None) == lib.W4_OK
+
+
+def test_linear_q4_f32_validation(lib):
+    r = lib.raw
+    f = lambda M=1, N=8, K=64, layout=0, sx=FAKE, xq=FAKE: r.w4_linear_q4_f32(
+        FAKE, FAKE, FAKE, FAKE, xq, sx, M, N, K, layout, None, 0, 0, None)
+    assert f(layout=3) == lib.W4_EINVAL
+    assert f(K=1000001) == lib.W4_ESHAPE
+    assert f(layout=1, N=100) == lib.W4_ESHAPE
+    assert f(sx=None) == lib.W4_EINVAL
+    assert f(xq=None) == lib.W4_EINVAL
+    assert f(M=0) == lib.W4_OK
+    assert f(M=-1) == lib.W4_EINVAL

@@ -162,6 +162,30 @@ def test_linear_q4_all_extreme(ops, M, K):
     assert np.all(y == np.float32(127 * 7 * K))
 
 
+@pytest.mark.parametrize("K", [16384, 65536, 131072])
+def test_linear_q4_extreme_long_rows(ops, ora, K):
+    """Extreme codes (x = +-127, nibbles 0 = -8 and 15 = +7) on rows long
+    enough that a warp's partial sums approach and pass 2^24: the integer
+    result must stay exact whichever accumulation the kernels pick."""
+    N, M = 1024, 2
+    xq = np.full((M, K), 127, np.int8)
+    xq[1, 1::2] = -127
+    w = np.zeros((N, K // 2), np.uint8)
+    w[1::2, ::3] = 0xFF
+    w[2::4, :] = 0xF0
+    sx = np.ones(M, np.float32)
+    sw = np.ones(N, np.float32)
+    want = ora.linear_q4(xq, sx, w, sw, K)
+    wd, swd = dev(w), dev(sw)
+    for flags in (0, ops.FLAG_PDL):
+        y = host(ops.linear_q4(dev(xq), dev(sx), wd, swd, K=K, flags=flags))
+        assert np.array_equal(bits(y), bits(want))
+    y, xq_d, sx_d = ops.linear_q4_f32(dev(xq.astype(np.float32)), wd, swd, K=K, flags=ops.FLAG_PDL)
+    assert np.array_equal(host(xq_d), xq) and np.all(host(sx_d) == 1.0)
+    assert np.array_equal(bits(host(y)), bits(want))
+    assert ops.device_status() == 0
+
+
 @pytest.mark.parametrize("M", [1, 3, 16])
 @pytest.mark.parametrize("N,K", [(1024, 1024), (37, 200), (3072, 1024), (64, 64)])
 def test_linear_q8_bitexact(ops, ora, M, N, K):

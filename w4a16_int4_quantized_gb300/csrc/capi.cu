@@ -151,6 +151,39 @@ w4_status w4_linear_q4(const int8_t *xq, const float *sx, const uint8_t *w, cons
     return run_linear(a, as_stream(stream));
 }
 
+w4_status w4_linear_q4_f32(const float *x, const uint8_t *w, const float *sw, float *y, int8_t *xq, float *sx,
+                           int64_t M, int64_t N, int64_t K, int32_t layout, void *workspace, size_t ws_bytes,
+                           uint32_t flags, void *stream) {
+    if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64) return W4_EINVAL;
+    if (K > kMaxKQ4 || M >= kMaxDim || N >= kMaxDim) return W4_ESHAPE;
+    if (layout == W4_LAYOUT_N64 && N % 64) return W4_ESHAPE;
+    if (M == 0) return W4_OK;
+    if (!sx || (K > 0 && (!x || !xq))) return W4_EINVAL;
+    if (N > 0 && (!y || !sw || (K > 0 && !w))) return W4_EINVAL;
+    const w4_status ws = check_workspace(W4_OP_LINEAR_Q4, M, N, K, 0, workspace, ws_bytes);
+    if (ws != W4_OK) return ws;
+    cudaStream_t st = as_stream(stream);
+    w4::LinearArgs a = {};
+    a.kind = w4::KIND_W4A8;
+    a.x = xq; a.w = w; a.scale = sw; a.sx = sx; a.y = y;
+    a.M = M; a.N = N; a.K = K; a.G = 0; a.layout = layout; a.flags = flags;
+    a.workspace = workspace; a.ws_bytes = ws_bytes;
+    if (N > 0 && K > 0 && M <= 8 && layout == W4_LAYOUT_ROWMAJOR && w4::gemv_supported(a)) {
+        uint32_t *status = nullptr;
+        const cudaError_t e = status_ptr(&status);
+        if (e != cudaSuccess) return cuda_status(e);
+        a.status = status;
+        a.xf = x; a.xq_out = xq; a.sx_out = sx;
+        return cuda_status(w4::launch_gemv(a, st));  // fused, or the quantizer then the linear
+    }
+    const cudaError_t e = w4::launch_quantize_rows(x, M, K, 127, xq, sx, nullptr, st);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (N == 0) return W4_OK;
+    if (K == 0) return cuda_status(cudaMemsetAsync(y, 0, (size_t)(M * N) * sizeof(float), st));
+    return run_linear(a, st);
+}
+
 w4_status w4_linear_q8(const int8_t *xq, const float *sx, const int8_t *w, const float *sw, float *y, int64_t M,
                        int64_t N, int64_t K, void *workspace, size_t ws_bytes, uint32_t flags, void *stream) {
     if (M < 0 || N < 0 || K < 0) return W4_EINVAL;

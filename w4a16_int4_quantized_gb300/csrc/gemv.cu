@@ -55,6 +55,24 @@ template <int KIND> constexpr bool kBiased = KIND == KIND_W4A8 || KIND == KIND_W
 template <int KIND> constexpr bool kW8 = KIND == KIND_W8A8 || KIND == KIND_W8A16;        // int8 weights, 32-B chunks
 template <int KIND> constexpr int kXPlanes = KIND == KIND_W8A16 ? 2 : 1;  // f32 x as bf16 hi + lo
 
+// Integer kinds: whether a warp may add its unit partials (exact integers in
+// f32) in f32 and convert once -- every partial sum of the warp is an integer
+// below 2^24 in magnitude, so each f32 addition is exact and the result is the
+// i32 sum.  Columns per warp times the largest |x code * weight code|.
+template <int KIND>
+W4_DEV bool f32_sum_exact(int units_per_warp, int unit_k) {
+    return (long long)units_per_warp * unit_k * 127 * (kW8<KIND> ? 128 : 8) < (1LL << 24);
+}
+
+// acc += part, exactly: in f32 (bits kept in the int) or per unit in i32.
+W4_DEV void add_exact(int &acc, float part, bool f32sum) {
+    if (f32sum) acc = __float_as_int(__int_as_float(acc) + part);
+    else acc += __float2int_rn(part);
+}
+W4_DEV void finish_exact(int &acc, bool f32sum) {
+    if (f32sum) acc = __float2int_rn(__int_as_float(acc));
+}
+
 struct GemvParams {
     const void *x;
     const uint8_t *w;
@@ -79,6 +97,10 @@ struct GemvParams {
     int sstride;     // shared row stride of the f32 scale tile (floats)
     int raw_off, w_off, x_off, sc_off, red_off, bar_off;
     int zc_off, xs_off;  // W4A8G: (8 - z) per [row][unit] (int), activation sums per [m][unit] (int)
+    const float *xf;  // fused W4A8: f32 activations [M][K], quantised per row in every CTA
+    int8_t *xq_out;   // fused W4A8: the Q8 codes [M][K] (written by CTA 0)
+    float *sx_out;    // fused W4A8: the row scales [M] (written by CTA 0)
+    int xq_off;       // fused W4A8: shared row scales [16] + per-warp row maxima [16 warps][8]
     int x_vec;       // activation rows can be read with aligned vector loads
     int s_vec;       // scale rows can be read as 16-byte vectors
 };
@@ -673,6 +695,7 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
     const int *zc0 = reinterpret_cast<const int *>(smem + p.zc_off) + (rbase + g) * p.sstride;
     const int *zc1 = reinterpret_cast<const int *>(smem + p.zc_off) + (rbase + g + 8) * p.sstride;
     const int *xsum = reinterpret_cast<const int *>(smem + p.xs_off);
+    const bool f32sum = kIntAcc<KIND> && f32_sum_exact<KIND>((nun + p.WK - 1) / p.WK, p.unit_k);
     // fold one unit's partial into acc (units arrive in increasing order)
     auto fold = [&](const float (&part)[MT][4], int u) {
         if constexpr (KIND == KIND_W4A8G) {
@@ -710,7 +733,7 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[mt][i] += __float2int_rn(part[mt][i]);
+                for (int i = 0; i < 4; ++i) add_exact(acc[mt][i], part[mt][i], f32sum);
         }
     };
     auto run_unit = [&](int u, int ul, float (&part)[MT][4]) {
@@ -766,6 +789,12 @@ __global__ void __launch_bounds__(512) gemv_kernel(const __grid_constant__ GemvP
         }
         if constexpr (N64) __syncthreads();  // the next phase overwrites the tile
     }
+    if constexpr (kIntAcc<KIND>) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) finish_exact(acc[mt][i], f32sum);
+    }
 
     combine_and_store<KIND, RB, MT>(p, acc, wr, wk, lane, g, t, row0 + rbase, smem);
 }
@@ -799,6 +828,7 @@ __global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant_
     const int rbase = wr * RB;
     // the warp's units: wk, wk + WK, ... of the CTA's span (gemv_kernel's order)
     const int nu_w = wk < nun ? (nun - wk + WK - 1) / WK : 0;
+    const bool f32sum = kInt && f32_sum_exact<KIND>((nun + WK - 1) / WK, p.unit_k);
     constexpr int kUW = NW / CPG;  // units held in registers per window
     // rows g and g + 8 of the warp's block, clamped to a valid row (clamped rows are never stored)
     const int rA = min(row0 + rbase + g, p.N - 1);
@@ -897,12 +927,166 @@ __global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant_
 #pragma unroll
                     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) acc[mt][i] += __float2int_rn(part[mt][i]);
+                        for (int i = 0; i < 4; ++i) add_exact(acc[mt][i], part[mt][i], f32sum);
                 }
             }
         }
     }
+    if constexpr (kInt) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) finish_exact(acc[mt][i], f32sum);
+    }
     combine_and_store<KIND, RB, MT>(p, acc, wr, wk, lane, g, t, row0 + rbase, smem);
+}
+
+// ---------------------------------------------------------------- fused Q8 quantisation
+
+// Q8 code of v for scale sx > 0 (quantize_row_q8: clamp(rint(fl(v / sx)), -127, 127)),
+// given r = fl(1 / sx) (finite).  t = fl(v * r) is within 2^-16 + 2^-24 of
+// x = v / sx when |x| < 256 (two correctly rounded operations, each within
+// 2^-24 relative), and fl(x) within ulp(x) / 2 <= 2^-17 of x, so t and fl(x)
+// lie within 2^-15 of each other.  When t is farther than 2^-13 from every
+// half-integer, rint(t) == rint(fl(x)); otherwise the IEEE quotient itself
+// is rounded.
+W4_DEV int q8_code_fast(float v, float sx, float r) {
+    const float t = __fmul_rn(v, r);
+    const float rt = rintf(t);
+    int q;
+    if (fabsf(t) < 256.0f && 0.5f - fabsf(t - rt) > 0x1p-13f) q = __float2int_rn(rt);
+    else q = __float2int_rn(__fdiv_rn(v, sx));
+    return min(max(q, -127), 127);
+}
+
+// W4A8 activations straight from f32 ("Q4 weights x Q8 activations"): every
+// CTA quantises the M <= 8 rows itself with quantize_row_q8's arithmetic
+// (amax over the row, sx = fl(amax / 127), codes clamp(rint(fl(v / sx)))),
+// and stages the codes as stage_x<KIND_W4A8> would (biased f16 pairs), the
+// row scales in shared memory.  CTA 0 also writes the codes and scales out.
+W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
+    // The code here runs once per launch: it is kept short (one division and
+    // one reciprocal in the common case, loops where unrolling buys nothing),
+    // as instruction fetch, not arithmetic, bounds it.
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = nthr >> 5;
+    float *sx_s = reinterpret_cast<float *>(smem + p.xq_off);
+    float *red = sx_s + 16;  // [warp][m]
+    const int K = p.K;
+    const bool write_out = blockIdx.x == 0 && p.xq_out != nullptr;
+    const uint32_t xsel4[4] = {0x0400u, 0x0501u, 0x0602u, 0x0703u};
+    // M = 1 with K % 8 == 0: every 4-column vector held in registers from
+    // the max pass to the code pass; lanes 2i, 2i + 1 hold the two halves of
+    // one 8-column group.
+    constexpr int kV = 4;
+    const int n4 = K >> 2;
+    const bool regs = p.M == 1 && p.x_vec && (K & 7) == 0 && n4 <= kV * nthr &&
+                      (!write_out || (reinterpret_cast<uintptr_t>(p.xq_out) & 7) == 0);
+    float4 v[kV];
+    if (regs) {
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kV; ++i) {
+            const int j = tid + i * nthr;
+            v[i] = j < n4 ? __ldg(reinterpret_cast<const float4 *>(p.xf) + j) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            am = fmaxf(am, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) red[warp * 8] = am;
+    } else {
+#pragma unroll 1
+        for (int m = 0; m < p.M; ++m) {
+            const float *xr = p.xf + (size_t)m * K;
+            float am = 0.0f;
+#pragma unroll 1
+            for (int k = tid; k < K; k += nthr) am = fmaxf(am, fabsf(xr[k]));
+#pragma unroll
+            for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+            if (lane == 0) red[warp * 8 + m] = am;
+        }
+    }
+    __syncthreads();
+    if (tid < p.M) {
+        float a = red[tid];
+#pragma unroll 1
+        for (int w2 = 1; w2 < nw; ++w2) a = fmaxf(a, red[w2 * 8 + tid]);
+        const float sx = __fdiv_rn(a, 127.0f);
+        sx_s[tid] = sx;
+        if (blockIdx.x == 0 && p.sx_out) p.sx_out[tid] = sx;
+    }
+    __syncthreads();
+    if (regs) {
+        // codes by t = fl(v * fl(1 / sx)) (see q8_code_fast); values whose t
+        // lies within 2^-13 of a half-integer (or all, when 1 / sx overflows)
+        // are redone with the IEEE quotient
+        const float sx = sx_s[0];
+        const float r = sx != 0.0f ? __frcp_rn(sx) : 0.0f;
+        const bool fast = isfinite(r);
+        uint32_t c4[kV];
+        uint32_t redo = 0;
+#pragma unroll
+        for (int i = 0; i < kV; ++i) {
+            c4[i] = 0;
+            const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float tq = __fmul_rn(e[q], r);
+                const float rt = rintf(tq);
+                const bool ok = fast && fabsf(tq) < 256.0f && 0.5f - fabsf(tq - rt) > 0x1p-13f;
+                const int c = ok ? min(max(__float2int_rn(rt), -127), 127) : 0;
+                c4[i] |= (uint32_t)(uint8_t)(int8_t)c << (8 * q);
+                if (!ok && sx != 0.0f) redo |= 1u << (4 * i + q);
+            }
+        }
+#pragma unroll 1
+        for (uint32_t rd = redo; rd; rd &= rd - 1) {
+            const int b = __ffs(rd) - 1, i = b >> 2, q = b & 3;
+            const float4 vi = i == 0 ? v[0] : i == 1 ? v[1] : i == 2 ? v[2] : v[3];
+            const float e = q == 0 ? vi.x : q == 1 ? vi.y : q == 2 ? vi.z : vi.w;
+            const uint32_t c = (uint32_t)(uint8_t)(int8_t)min(max(__float2int_rn(__fdiv_rn(e, sx)), -127), 127);
+            const uint32_t bits = c << (8 * q);
+            c4[0] |= i == 0 ? bits : 0u;
+            c4[1] |= i == 1 ? bits : 0u;
+            c4[2] |= i == 2 ? bits : 0u;
+            c4[3] |= i == 3 ? bits : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < kV; ++i) {
+            // exchange the 4 codes with the partner lane (the other half of the 8-column group)
+            const int j = tid + i * nthr;
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, c4[i], 1);
+            if (j < n4 && (j & 1) == 0) {
+                if (write_out) *reinterpret_cast<uint2 *>(p.xq_out + 4 * j) = make_uint2(c4[i], other);
+                uint32_t b[4];
+                s8_to_f16_pairs(c4[i], other, xsel4, b);
+                *reinterpret_cast<uint4 *>(smem + p.x_off + 8 * j) = make_uint4(b[0], b[1], b[2], b[3]);
+            }
+        }
+    } else {
+        // one 8-column group per step; zero codes beyond K
+        const int per_row = (p.units * p.unit_k) >> 3;
+        const uint32_t pr_magic = div_magic((uint32_t)per_row);
+#pragma unroll 1
+        for (int j = tid; j < p.M * per_row; j += nthr) {
+            const int m = fast_div(j, pr_magic), b8 = j - m * per_row;
+            const float *xr = p.xf + (size_t)m * K;
+            const float sx = sx_s[m];
+            uint32_t lohi[2] = {0u, 0u};
+#pragma unroll 1
+            for (int i = 0; i < 8; ++i) {
+                const int k = 8 * b8 + i;
+                int c = 0;
+                if (k < K && sx != 0.0f) c = min(max(__float2int_rn(__fdiv_rn(xr[k], sx)), -127), 127);
+                if (k < K && write_out) p.xq_out[(size_t)m * K + k] = (int8_t)c;
+                const uint32_t bits = (uint32_t)(uint8_t)(int8_t)c << (8 * (i & 3));
+                if (i < 4) lohi[0] |= bits;
+                else lohi[1] |= bits;
+            }
+            uint32_t b[4];
+            s8_to_f16_pairs(lohi[0], lohi[1], xsel4, b);
+            *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) = make_uint4(b[0], b[1], b[2], b[3]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------- streaming kernel
@@ -922,9 +1106,10 @@ __global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant_
 // The K split (WK warps, one split per row), the unit -> warp assignment, the
 // MMA operand order, the fold and the combine order are gemv_kernel's, so the
 // results are bit-identical to it (and so across M and layouts).
-template <int KIND, int RB, int CPG, int NRBW>
+template <int KIND, int RB, int CPG, int NRBW, bool XQ>
 __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
     static_assert(KIND == KIND_W4A16 || KIND == KIND_W4A8, "row-major int4 kinds");
+    static_assert(!XQ || KIND == KIND_W4A8, "fused quantisation is W4A8's");
     griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool kInt = kIntAcc<KIND>;
@@ -955,7 +1140,8 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
     const bool svec = prefetch_scales<KIND>(p, row0, rows, 0, nun, nthr, sv, smem);
 
     griddep_wait();  // x may be written, and y read, by the previous kernel
-    stage_x<KIND>(p, 0, nun * p.unit_k, nthr, smem);
+    if constexpr (XQ) stage_x_q8(p, nthr, smem);
+    else stage_x<KIND>(p, 0, nun * p.unit_k, nthr, smem);
     store_scales<KIND>(p, rows, nun, nthr, svec, sv, smem);
     __syncthreads();
 
@@ -971,6 +1157,7 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
     const float *scf = reinterpret_cast<const float *>(smem + p.sc_off);
     const int WK = p.WK;
     const int cpg = CPG > 0 ? CPG : p.cpg;
+    const bool f32sum = kInt && f32_sum_exact<KIND>((nun + WK - 1) / WK, p.unit_k);
     bool ok = true;
 #pragma unroll
     for (int j = 0; j < NRBW; ++j) {
@@ -994,7 +1181,7 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
                 acc[j][3] = fmaf(s1, part[0][3], acc[j][3]);
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) acc[j][i] += __float2int_rn(part[0][i]);
+                for (int i = 0; i < 4; ++i) add_exact(acc[j][i], part[0][i], f32sum);
             }
         };
         auto run_unit = [&](int u, float (&part)[1][4]) {
@@ -1004,6 +1191,31 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
             unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, part);
         };
         int u = wk;
+        if (kInt && f32sum) {
+            // every partial sum of the warp is an integer below 2^24: the MMA
+            // accumulators run across units (four chains), added once at the end
+            float chain[4][1][4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) chain[q][0][i] = 0.0f;
+            for (; u + 3 * WK < nun; u += 4 * WK) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint8_t *xr[1] = {xrow + 64 * cpg * (u + q * WK)};
+                    unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * (u + q * WK), g, t, 0, xr, xvalid, cpg,
+                                                      chain[q]);
+                }
+            }
+            for (int q = 0; u < nun; u += WK, ++q) {
+                const uint8_t *xr[1] = {xrow + 64 * cpg * u};
+                unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, chain[0]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc[j][i] = __float2int_rn((chain[0][0][i] + chain[1][0][i]) + (chain[2][0][i] + chain[3][0][i]));
+            continue;
+        }
         for (; u + 3 * WK < nun; u += 4 * WK) {
             float part[4][1][4];
 #pragma unroll
@@ -1015,6 +1227,10 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
             float part[1][4];
             run_unit(u, part);
             fold(part, u);
+        }
+        if constexpr (kInt) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) finish_exact(acc[j][i], f32sum);
         }
     }
     if (!ok) {
@@ -1060,7 +1276,8 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
             float out;
             if constexpr (kInt) {
                 const float sw = static_cast<const float *>(p.scale)[n];
-                out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[j][i]), p.sx[m]), sw);
+                const float sxm = XQ ? reinterpret_cast<const float *>(smem + p.xq_off)[m] : p.sx[m];
+                out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[j][i]), sxm), sw);
             } else {
                 out = acc[j][i];
             }
@@ -1222,11 +1439,11 @@ cudaError_t launch_direct(const GemvParams &p, int S, int threads, int smem, cud
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int KIND, int RB, int CPG, int NRBW>
+template <int KIND, int RB, int CPG, int NRBW, bool XQ = false>
 cudaError_t launch_stream(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    auto *kern = gemv_stream_kernel<KIND, RB, CPG, NRBW>;
+    auto *kern = gemv_stream_kernel<KIND, RB, CPG, NRBW, XQ>;
     std::call_once(once, [kern] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
@@ -1244,20 +1461,20 @@ cudaError_t launch_stream(const GemvParams &p, int threads, int smem, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int KIND, int RB, int CPG>
+template <int KIND, int RB, int CPG, bool XQ>
 cudaError_t dispatch_stream_nrbw(const GemvParams &p, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
     switch (nrbw) {
-        case 1: return launch_stream<KIND, RB, CPG, 1>(p, threads, smem, st, pdl);
-        case 2: return launch_stream<KIND, RB, CPG, 2>(p, threads, smem, st, pdl);
-        case 3: return launch_stream<KIND, RB, CPG, 3>(p, threads, smem, st, pdl);
-        default: return launch_stream<KIND, RB, CPG, 4>(p, threads, smem, st, pdl);
+        case 1: return launch_stream<KIND, RB, CPG, 1, XQ>(p, threads, smem, st, pdl);
+        case 2: return launch_stream<KIND, RB, CPG, 2, XQ>(p, threads, smem, st, pdl);
+        case 3: return launch_stream<KIND, RB, CPG, 3, XQ>(p, threads, smem, st, pdl);
+        default: return launch_stream<KIND, RB, CPG, 4, XQ>(p, threads, smem, st, pdl);
     }
 }
 
-template <int KIND, int CPG>
+template <int KIND, int CPG, bool XQ = false>
 cudaError_t dispatch_stream(const GemvParams &p, int rb, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
-    if (rb == 16) return dispatch_stream_nrbw<KIND, 16, CPG>(p, nrbw, threads, smem, st, pdl);
-    return dispatch_stream_nrbw<KIND, 8, CPG>(p, nrbw, threads, smem, st, pdl);
+    if (rb == 16) return dispatch_stream_nrbw<KIND, 16, CPG, XQ>(p, nrbw, threads, smem, st, pdl);
+    return dispatch_stream_nrbw<KIND, 8, CPG, XQ>(p, nrbw, threads, smem, st, pdl);
 }
 
 template <int KIND, int CPG>
@@ -1369,7 +1586,7 @@ bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out,
     p.sstride = p.upc | 1;
     const int xbytes = (int)round_up((int64_t)a.M * p.xstride, 128);
     const int per_row = p.wstride + (a.kind == KIND_W4A16 ? 4 * p.sstride : 0);
-    const int fixed = 128 + xbytes + 2 * 128;
+    const int fixed = 128 + xbytes + 2 * 128 + (a.xf ? 640 : 0);
     // rows per CTA: the fewest waves of 152 CTAs, rows spread evenly, a whole number of RB-row blocks
     auto rows_for = [&](int RB) -> int {
         const int rmax = std::min((kStreamSmemPerCta - fixed) / per_row / RB * RB, kStreamMaxBlocks * RB);
@@ -1396,6 +1613,8 @@ bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out,
     off += xbytes;
     p.sc_off = off;
     if (a.kind == KIND_W4A16) off += (int)round_up((int64_t)R * p.sstride * 4, 128);
+    p.xq_off = off;
+    if (a.xf) off += 640;  // 16 row scales + 16 warps x 8 row maxima (f32)
     // the K-split combine reuses the weight tile once every warp is done with it
     const int red = (p.WK - 1) * WR * nrbw * 32 * 16;
     p.red_off = p.w_off;
@@ -1483,6 +1702,23 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
         s.WR = 1;
         if (a.M >= 4)
             while (s.WR < 4 && a.N / (s.RB * s.WR * 2) >= 2 * 152) s.WR *= 2;
+    }
+    // Fused W4A8 (f32 activations quantised in every CTA): the streaming
+    // kernel when it applies, else the row quantizer and then this path.
+    if (a.xf) {
+        GemvParams q = p;
+        q.WK = s.WK;
+        int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
+        if (a.kind == KIND_W4A8 && S == 1 && plan_stream(a, q, rb, nrbw, sthreads, ssmem) &&
+            ceil_div(a.N, (int64_t)q.R) >= 120) {
+            q.xf = a.xf;
+            q.xq_out = a.xq_out;
+            q.sx_out = a.sx_out;
+            q.x_vec = (a.K % 4 == 0 && reinterpret_cast<uintptr_t>(a.xf) % 16 == 0) ? 1 : 0;
+            return dispatch_stream<KIND_W4A8, 1, true>(q, rb, nrbw, sthreads, ssmem, st, (a.flags & W4_FLAG_PDL) != 0);
+        }
+        const cudaError_t e = launch_quantize_rows(a.xf, a.M, a.K, 127, a.xq_out, a.sx_out, nullptr, st);
+        if (e != cudaSuccess) return e;
     }
     const int smem = plan_smem(a, s, p);
     if (smem > kSmemLimit) return launch_generic(a, st);

@@ -30,6 +30,11 @@ struct LinearArgs {
     void *workspace;
     size_t ws_bytes;
     uint32_t *status;    // device status word
+    // fused W4A8 (w4_linear_q4_f32): f32 activations quantised inside the
+    // linear; x / sx then name the buffers that receive the codes and scales
+    const float *xf;
+    int8_t *xq_out;
+    float *sx_out;
 };
 
 // tmap.cu -- TMA tensor map of a tiled box (rank <= 5); strides of dims 1..rank-1 in bytes.

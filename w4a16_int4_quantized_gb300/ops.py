@@ -40,6 +40,7 @@ SIGNATURES = [
     ("w4_quantize_matrix_q8", _i32, [_vp, _i64, _i64, _vp, _vp, _vp]),
     ("w4_dot_i32_q4", _i32, [_vp, _vp, _i64, _vp, _vp]),
     ("w4_linear_q4", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
+    ("w4_linear_q4_f32", _i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q8", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_w4a16_group", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_noalloc", _i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
@@ -163,6 +164,22 @@ def linear_q4(xq, sx, w, sw, K: int | None = None, N: int | None = None, layout:
     _check(raw.w4_linear_q4(_ptr(xq), _ptr(sx), _ptr(w), _ptr(sw), _ptr(y), M, N, K, layout,
                             _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_q4")
     return y
+
+
+def linear_q4_f32(x, w, sw, K: int | None = None, N: int | None = None, layout: int = LAYOUT_ROWMAJOR,
+                  flags: int = 0, out=None, xq=None, sx=None, workspace=None, stream=None):
+    """quantize_row_q8(x) then linear_q4 in one call -> (y [M, N], xq [M, K], sx [M])."""
+    assert x.dtype == torch.float32 and x.dim() == 2
+    M = x.shape[0]
+    K = x.shape[1] if K is None else K
+    N = sw.numel() if N is None else N
+    y = out if out is not None else torch.empty((M, N), dtype=torch.float32, device=x.device)
+    xq = xq if xq is not None else torch.empty((M, K), dtype=torch.int8, device=x.device)
+    sx = sx if sx is not None else torch.empty(M, dtype=torch.float32, device=x.device)
+    ws, wsb = _workspace(OP_LINEAR_Q4, M, N, K, 0, workspace, x.device)
+    _check(raw.w4_linear_q4_f32(_ptr(x), _ptr(w), _ptr(sw), _ptr(y), _ptr(xq), _ptr(sx), M, N, K, layout,
+                                _ptr(ws), wsb, flags, _stream(stream)), "w4_linear_q4_f32")
+    return y, xq, sx
 
 
 NOALLOC_SCRATCH_BYTES = 8 << 20
