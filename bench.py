@@ -98,7 +98,8 @@ WORKLOADS = {
 # DRAM bytes (read + write) per launch of the roofline's kernel from one ncu
 # capture (profiles/); None where no capture matches the current kernel.
 TRAFFIC = {
-    "w4a16_gemv_m1": 2395392,                 # profiles/gemv_w4a16_m1_n2048_k2048.md
+    "w4a16_gemv_m1": 2393856,                 # profiles/gemv_w4a16_m1_n2048_k2048.md
+    "w4a8_gemv_m1": 2161408,                  # profiles/gemv_w4a8_fused_m1_n2048_k2048.md
 }
 
 
@@ -118,7 +119,9 @@ def weight_bytes(w) -> int:
 def step_bytes(w) -> int:
     """Algorithmic bytes of one linear launch: weights + scales + activations + output."""
     M, N, K = w["M"], w["N"], w["K"]
-    xb = {"w4a16": M * K * 2, "w8a16": M * K * 4}.get(w["kind"], M * K + 4 * M)
+    # x side: bf16 x (W4A16); f32 x (W8A16); f32 x in, Q8 codes and scales out (W4A8);
+    # Q8 codes and scales in (grouped W4A8, quantised by a separate call)
+    xb = {"w4a16": M * K * 2, "w8a16": M * K * 4, "w4a8": 5 * M * K + 4 * M}.get(w["kind"], M * K + 4 * M)
     return weight_bytes(w) + xb + M * N * 4
 
 
