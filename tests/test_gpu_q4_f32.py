@@ -86,3 +86,18 @@ def test_linear_q4_f32_ties_and_zero_rows(ops, ora):
     x[2, :] = np.float32(1e-40) * ((np.arange(K) % 5) - 2)
     W = synth.weights_f32(181, 2048, K)
     check(ops, ora, x, W, flags=1)
+    for m in range(3):  # alone: the one-row integer-dot kernel
+        check(ops, ora, np.ascontiguousarray(x[m:m + 1]), W, flags=1)
+
+
+@pytest.mark.parametrize("K", [32, 1024, 2048, 2047, 4096, 4128])
+def test_linear_q4_one_row(ops, ora, K):
+    """M = 1 through both entry points with PDL (the integer-dot kernel where
+    K allows), against the oracle's bits."""
+    x = synth.activations_f32(191 + K, 1, K)
+    W = synth.weights_f32(192 + K, 2048, K)
+    check(ops, ora, x, W, flags=1)
+    xq, sx, _ = ora.quantize_row_q8(x)
+    wq, sw = ora.quantize_matrix_q4(W)
+    y = host(ops.linear_q4(dev(xq), dev(sx), dev(wq), dev(sw), K=K, flags=ops.FLAG_PDL))
+    assert np.array_equal(bits(y), bits(ora.linear_q4(xq, sx, wq, sw, K)))

@@ -101,6 +101,7 @@ struct GemvParams {
     int8_t *xq_out;   // fused W4A8: the Q8 codes [M][K] (written by CTA 0)
     float *sx_out;    // fused W4A8: the row scales [M] (written by CTA 0)
     int xq_off;       // fused W4A8: shared row scales [16] + per-warp row maxima [16 warps][8]
+    int rb;           // streaming kernels: rows per mbarrier block
     int x_vec;       // activation rows can be read with aligned vector loads
     int s_vec;       // scale rows can be read as 16-byte vectors
 };
@@ -964,6 +965,41 @@ W4_DEV int q8_code_fast(float v, float sx, float r) {
 // (amax over the row, sx = fl(amax / 127), codes clamp(rint(fl(v / sx)))),
 // and stages the codes as stage_x<KIND_W4A8> would (biased f16 pairs), the
 // row scales in shared memory.  CTA 0 also writes the codes and scales out.
+// Codes k0..k7 of an 8-column group (lo: k0..k3, hi: k4..k7) -> the staged
+// form of the integer-dot kernel: the even columns (k0 k2 k4 k6) then the odd
+// ones (k1 k3 k5 k7), matching the low and high nibbles of a weight word.
+W4_DEV uint2 even_odd(uint32_t lo, uint32_t hi) { return make_uint2(prmt(lo, hi, 0x6420u), prmt(lo, hi, 0x7531u)); }
+
+// One 16-byte weight chunk (32 columns: word j holds columns 8j..8j+7, low
+// nibbles even, high nibbles odd) against the chunk's even / odd codes.
+W4_DEV int dot_chunk_dp(uint4 w, uint4 xe, uint4 xo, int acc) {
+    const uint32_t m = 0x0F0F0F0Fu;
+    acc = __dp4a((int)(w.x & m), (int)xe.x, acc);
+    acc = __dp4a((int)((w.x >> 4) & m), (int)xo.x, acc);
+    acc = __dp4a((int)(w.y & m), (int)xe.y, acc);
+    acc = __dp4a((int)((w.y >> 4) & m), (int)xo.y, acc);
+    acc = __dp4a((int)(w.z & m), (int)xe.z, acc);
+    acc = __dp4a((int)((w.z >> 4) & m), (int)xo.z, acc);
+    acc = __dp4a((int)(w.w & m), (int)xe.w, acc);
+    acc = __dp4a((int)((w.w >> 4) & m), (int)xo.w, acc);
+    return acc;
+}
+
+// Sum of the 32 codes of a chunk.
+W4_DEV int sum_chunk_dp(uint4 xe, uint4 xo, int acc) {
+    const int one = 0x01010101;
+    acc = __dp4a((int)xe.x, one, acc);
+    acc = __dp4a((int)xe.y, one, acc);
+    acc = __dp4a((int)xe.z, one, acc);
+    acc = __dp4a((int)xe.w, one, acc);
+    acc = __dp4a((int)xo.x, one, acc);
+    acc = __dp4a((int)xo.y, one, acc);
+    acc = __dp4a((int)xo.z, one, acc);
+    acc = __dp4a((int)xo.w, one, acc);
+    return acc;
+}
+
+template <bool DP>
 W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
     // The code here runs once per launch: it is kept short (one division and
     // one reciprocal in the common case, loops where unrolling buys nothing),
@@ -1057,9 +1093,13 @@ W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
             const uint32_t other = __shfl_xor_sync(0xffffffffu, c4[i], 1);
             if (j < n4 && (j & 1) == 0) {
                 if (write_out) *reinterpret_cast<uint2 *>(p.xq_out + 4 * j) = make_uint2(c4[i], other);
-                uint32_t b[4];
-                s8_to_f16_pairs(c4[i], other, xsel4, b);
-                *reinterpret_cast<uint4 *>(smem + p.x_off + 8 * j) = make_uint4(b[0], b[1], b[2], b[3]);
+                if constexpr (DP) {
+                    *reinterpret_cast<uint2 *>(smem + p.x_off + 4 * j) = even_odd(c4[i], other);
+                } else {
+                    uint32_t b[4];
+                    s8_to_f16_pairs(c4[i], other, xsel4, b);
+                    *reinterpret_cast<uint4 *>(smem + p.x_off + 8 * j) = make_uint4(b[0], b[1], b[2], b[3]);
+                }
             }
         }
     } else {
@@ -1082,9 +1122,14 @@ W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
                 if (i < 4) lohi[0] |= bits;
                 else lohi[1] |= bits;
             }
-            uint32_t b[4];
-            s8_to_f16_pairs(lohi[0], lohi[1], xsel4, b);
-            *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) = make_uint4(b[0], b[1], b[2], b[3]);
+            if constexpr (DP) {
+                *reinterpret_cast<uint2 *>(smem + p.x_off + m * p.xstride + 8 * b8) = even_odd(lohi[0], lohi[1]);
+            } else {
+                uint32_t b[4];
+                s8_to_f16_pairs(lohi[0], lohi[1], xsel4, b);
+                *reinterpret_cast<uint4 *>(smem + p.x_off + m * p.xstride + 16 * b8) =
+                    make_uint4(b[0], b[1], b[2], b[3]);
+            }
         }
     }
 }
@@ -1140,7 +1185,7 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
     const bool svec = prefetch_scales<KIND>(p, row0, rows, 0, nun, nthr, sv, smem);
 
     griddep_wait();  // x may be written, and y read, by the previous kernel
-    if constexpr (XQ) stage_x_q8(p, nthr, smem);
+    if constexpr (XQ) stage_x_q8<false>(p, nthr, smem);
     else stage_x<KIND>(p, 0, nun * p.unit_k, nthr, smem);
     store_scales<KIND>(p, rows, nun, nthr, svec, sv, smem);
     __syncthreads();
@@ -1283,6 +1328,119 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
             }
             p.y[(size_t)m * p.N + n] = out;
         }
+    }
+}
+
+// ---------------------------------------------------------------- W4A8, one activation row
+//
+// linear_q4 at M = 1 by integer dot products ("Q4 weights x Q8
+// activations": acc = sum_k xq * u - 8 * sum_k xq, exact in i32).  The data
+// movement is the streaming kernel's (whole-SM row ranges by bulk copies
+// before the PDL wait, the trigger at entry, two CTAs per SM); the
+// arithmetic is integer, so any order gives the same result.  One warp per
+// row: each lane takes 16-byte weight chunks (32 columns) and dp4a's the
+// low and high nibbles of each word against the even and odd activation
+// codes of that chunk, which it holds in registers for all its rows; the
+// warp sums its lanes.  At M = 1 the m16n8 MMA would leave 7 of its 8
+// columns idle and the f16 unpack would cost the integer pipe three times
+// as much.  XQ: the activations arrive as f32 and every CTA quantises them
+// (stage_x_q8); otherwise as Q8 codes.
+template <bool XQ, int XR>
+__global__ void __launch_bounds__(512, 2) gemv_q4dp_kernel(const __grid_constant__ GemvParams p) {
+    griddep_launch_dependents();
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int nthr = blockDim.x;
+    const int row0 = blockIdx.x * p.R;
+    const int rows = min(p.R, p.N - row0);
+    const int RB = p.rb;
+    const int nrb = (rows + RB - 1) / RB;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+
+    if (tid == 0) {
+        for (int b = 0; b < nrb; ++b) mbar_init(&bars[b], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            for (int b = 0; b < nrb; ++b) mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(RB, rows - b * RB) * p.Kb));
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb, &bars[r / RB]);
+    }
+
+    griddep_wait();  // x may be written, and y read, by the previous kernel
+    if constexpr (XQ) {
+        stage_x_q8<true>(p, nthr, smem);
+    } else {
+        const int8_t *xr = static_cast<const int8_t *>(p.x);
+        const int groups = p.Kb >> 2;  // 8-column groups (K padded to Kp)
+        for (int b8 = tid; b8 < groups; b8 += nthr) {
+            const int kk = 8 * b8;
+            uint32_t lo = 0, hi = 0;
+            if (p.x_vec && kk + 8 <= p.K) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(xr + kk));
+                lo = v.x;
+                hi = v.y;
+            } else {
+#pragma unroll 1
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t b = kk + i < p.K ? (uint32_t)(uint8_t)xr[kk + i] : 0u;
+                    if (i < 4) lo |= b << (8 * i);
+                    else hi |= b << (8 * (i - 4));
+                }
+            }
+            *reinterpret_cast<uint2 *>(smem + p.x_off + 8 * b8) = even_odd(lo, hi);
+        }
+    }
+    __syncthreads();
+
+    // the lane's activation chunks (c = lane + 32 i), and the sum of all codes
+    const int chunks = p.Kb >> 4;
+    uint4 xe[XR], xo[XR];
+    int xs = 0;
+#pragma unroll
+    for (int i = 0; i < XR; ++i) {
+        const int c = lane + 32 * i;
+        xe[i] = make_uint4(0u, 0u, 0u, 0u);
+        xo[i] = xe[i];
+        if (c < chunks) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(smem + p.x_off + 32 * c);
+            const uint4 b = *reinterpret_cast<const uint4 *>(smem + p.x_off + 32 * c + 16);
+            xe[i] = make_uint4(a.x, a.z, b.x, b.z);
+            xo[i] = make_uint4(a.y, a.w, b.y, b.w);
+        }
+        xs = sum_chunk_dp(xe[i], xo[i], xs);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o);
+    const float sx = XQ ? reinterpret_cast<const float *>(smem + p.xq_off)[0] : p.sx[0];
+    const float *sw = static_cast<const float *>(p.scale);
+
+    bool ok = true;
+    for (int r = warp; r < rows; r += nw) {
+        if (!mbar_wait_bounded(&bars[r / RB], 0)) {
+            ok = false;
+            continue;
+        }
+        const uint8_t *wrow = smem + p.w_off + r * p.wstride;
+        int acc = 0;
+#pragma unroll
+        for (int i = 0; i < XR; ++i) {
+            const int c = lane + 32 * i;
+            if (c < chunks) acc = dot_chunk_dp(*reinterpret_cast<const uint4 *>(wrow + 16 * c), xe[i], xo[i], acc);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) {
+            const int n = row0 + r;
+            p.y[n] = __fmul_rn(__fmul_rn(__int2float_rn(acc - 8 * xs), sx), sw[n]);
+        }
+    }
+    if (!ok) {
+        if (lane == 0 && p.status) atomicOr(p.status, kStatusCopyTimeout);
+        for (int b = warp; b < nrb; b += nw) (void)mbar_wait_bounded(&bars[b], 0);
     }
 }
 
@@ -1475,6 +1633,41 @@ template <int KIND, int CPG, bool XQ = false>
 cudaError_t dispatch_stream(const GemvParams &p, int rb, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
     if (rb == 16) return dispatch_stream_nrbw<KIND, 16, CPG, XQ>(p, nrbw, threads, smem, st, pdl);
     return dispatch_stream_nrbw<KIND, 8, CPG, XQ>(p, nrbw, threads, smem, st, pdl);
+}
+
+template <bool XQ, int XR>
+cudaError_t launch_q4dp(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    auto *kern = gemv_q4dp_kernel<XQ, XR>;
+    std::call_once(once, [kern] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(p.N, p.R), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+// Warps of the integer-dot kernel: about one per 4 rows of the CTA, 4 to 16
+// (measured: 4 warps for 16 rows and 16 for 88 rows beat the other choice).
+int q4dp_threads(int R) { return 32 * std::max(4, std::min(16, R / 4)); }
+
+// W4A8, M = 1, row-major, no K split, K <= 4096: the integer-dot kernel.
+template <bool XQ>
+cudaError_t dispatch_q4dp(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+    const int chunks = p.Kb >> 4;
+    if (chunks <= 32) return launch_q4dp<XQ, 1>(p, threads, smem, st, pdl);
+    if (chunks <= 64) return launch_q4dp<XQ, 2>(p, threads, smem, st, pdl);
+    return launch_q4dp<XQ, 4>(p, threads, smem, st, pdl);
 }
 
 template <int KIND, int CPG>
@@ -1715,7 +1908,10 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
             q.xq_out = a.xq_out;
             q.sx_out = a.sx_out;
             q.x_vec = (a.K % 4 == 0 && reinterpret_cast<uintptr_t>(a.xf) % 16 == 0) ? 1 : 0;
-            return dispatch_stream<KIND_W4A8, 1, true>(q, rb, nrbw, sthreads, ssmem, st, (a.flags & W4_FLAG_PDL) != 0);
+            q.rb = rb;
+            const bool qpdl = (a.flags & W4_FLAG_PDL) != 0;
+            if (a.M == 1 && (q.Kb >> 4) <= 128) return dispatch_q4dp<true>(q, q4dp_threads(q.R), ssmem, st, qpdl);
+            return dispatch_stream<KIND_W4A8, 1, true>(q, rb, nrbw, sthreads, ssmem, st, qpdl);
         }
         const cudaError_t e = launch_quantize_rows(a.xf, a.M, a.K, 127, a.xq_out, a.sx_out, nullptr, st);
         if (e != cudaSuccess) return e;
@@ -1729,6 +1925,15 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     s.S = S;
     const int threads = 32 * p.WR * p.WK;
     const bool pdl = (a.flags & W4_FLAG_PDL) != 0;
+    // W4A8, M = 1, large N, no K split, PDL: the integer-dot streaming kernel.
+    if (pdl && a.kind == KIND_W4A8 && a.M == 1 && a.layout == W4_LAYOUT_ROWMAJOR && S == 1 && (p.Kb >> 4) <= 128) {
+        GemvParams q = p;
+        int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
+        if (plan_stream(a, q, rb, nrbw, sthreads, ssmem) && ceil_div(a.N, (int64_t)q.R) >= 120) {
+            q.rb = rb;
+            return dispatch_q4dp<false>(q, q4dp_threads(q.R), ssmem, st, pdl);
+        }
+    }
     // Large N, M <= 8, no K split, PDL: the streaming kernel (same arithmetic).
     // Without PDL its per-row bulk copies have nothing to overlap with, and
     // the staged kernel's register loads reach HBM sooner.
