@@ -99,7 +99,7 @@ WORKLOADS = {
 # capture (profiles/); None where no capture matches the current kernel.
 TRAFFIC = {
     "w4a16_gemv_m1": 2393856,                 # profiles/gemv_w4a16_m1_n2048_k2048.md
-    "w4a8_gemv_m1": 2161408,                  # profiles/gemv_w4a8_fused_m1_n2048_k2048.md
+    "w4a8_gemv_m1": 2141184,                  # profiles/gemv_w4a8_fused_m1_n2048_k2048.md
 }
 
 
