@@ -269,7 +269,7 @@ def test_w4a16_batch_invariance(ops, N, K, G):
         assert np.array_equal(bits(y1[0]), bits(yb[m])), m
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
 @pytest.mark.parametrize("N,K,G", [(2048, 2048, 32), (2048, 2047, 32), (13312, 2048, 128), (1024, 1024, 128),
                                    (3072, 2048, 128), (4096, 8192, 128), (1000, 4096, 32)])
 def test_w4a16_pdl_same_bits(ops, ora, M, N, K, G):
@@ -286,7 +286,7 @@ def test_w4a16_pdl_same_bits(ops, ora, M, N, K, G):
     assert ops.device_status() == 0
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 @pytest.mark.parametrize("N,K", [(2048, 2048), (13312, 2048)])
 def test_linear_q4_pdl_bitexact(ops, ora, M, N, K):
     """The PDL-launched row quantizer followed by a PDL linear: the oracle's bits."""

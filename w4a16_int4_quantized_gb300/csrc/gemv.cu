@@ -1151,10 +1151,10 @@ W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
 // The K split (WK warps, one split per row), the unit -> warp assignment, the
 // MMA operand order, the fold and the combine order are gemv_kernel's, so the
 // results are bit-identical to it (and so across M and layouts).
-template <int KIND, int RB, int CPG, int NRBW, bool XQ>
-__global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
+template <int KIND, int RB, int CPG, int NRBW, bool XQ, int MT = 1>
+__global__ void __launch_bounds__(512, MT == 1 ? 2 : 1) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
     static_assert(KIND == KIND_W4A16 || KIND == KIND_W4A8, "row-major int4 kinds");
-    static_assert(!XQ || KIND == KIND_W4A8, "fused quantisation is W4A8's");
+    static_assert(!XQ || (KIND == KIND_W4A8 && MT == 1), "fused quantisation is W4A8's, M <= 8");
     griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool kInt = kIntAcc<KIND>;
@@ -1192,13 +1192,21 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
 
     // ---- 2. the warp's row blocks, in order, as they land.
     using Acc = typename std::conditional<kInt, int, float>::type;
-    Acc acc[NRBW][4];
+    Acc acc[NRBW][MT][4];
 #pragma unroll
     for (int j = 0; j < NRBW; ++j)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) acc[j][i] = 0;
-    const bool xvalid[1] = {g < p.M};
-    const uint8_t *xrow = smem + p.x_off + (xvalid[0] ? g : 0) * p.xstride + 16 * t;
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[j][mt][i] = 0;
+    bool xvalid[MT];
+    const uint8_t *xrow[MT];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const int m = g + 8 * mt;
+        xvalid[mt] = m < p.M;
+        xrow[mt] = smem + p.x_off + (xvalid[mt] ? m : 0) * p.xstride + 16 * t;
+    }
     const float *scf = reinterpret_cast<const float *>(smem + p.sc_off);
     const int WK = p.WK;
     const int cpg = CPG > 0 ? CPG : p.cpg;
@@ -1216,66 +1224,87 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
         const uint8_t *wrow8 = wrow + 8 * p.wstride;
         const float *sc0 = scf + (rb * RB + g) * p.sstride;
         const float *sc1 = scf + (rb * RB + g + 8) * p.sstride;
-        auto fold = [&](const float (&part)[1][4], int u) {
+        auto fold = [&](const float (&part)[MT][4], int u) {
             if constexpr (KIND == KIND_W4A16) {
                 const float s0 = sc0[u];
                 const float s1 = (RB == 16) ? sc1[u] : 0.0f;
-                acc[j][0] = fmaf(s0, part[0][0], acc[j][0]);
-                acc[j][1] = fmaf(s0, part[0][1], acc[j][1]);
-                acc[j][2] = fmaf(s1, part[0][2], acc[j][2]);
-                acc[j][3] = fmaf(s1, part[0][3], acc[j][3]);
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) {
+                    acc[j][mt][0] = fmaf(s0, part[mt][0], acc[j][mt][0]);
+                    acc[j][mt][1] = fmaf(s0, part[mt][1], acc[j][mt][1]);
+                    acc[j][mt][2] = fmaf(s1, part[mt][2], acc[j][mt][2]);
+                    acc[j][mt][3] = fmaf(s1, part[mt][3], acc[j][mt][3]);
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) add_exact(acc[j][i], part[0][i], f32sum);
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) add_exact(acc[j][mt][i], part[mt][i], f32sum);
             }
         };
-        auto run_unit = [&](int u, float (&part)[1][4]) {
+        auto run_unit = [&](int u, float (&part)[MT][4]) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) part[0][i] = 0.0f;
-            const uint8_t *xr[1] = {xrow + 64 * cpg * u};
-            unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, part);
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) part[mt][i] = 0.0f;
+            const uint8_t *xr[MT];
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) xr[mt] = xrow[mt] + 64 * cpg * u;
+            unit_mma<KIND, false, RB, MT, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, part,
+                                                p.M * p.xstride);
         };
         int u = wk;
         if (kInt && f32sum) {
             // every partial sum of the warp is an integer below 2^24: the MMA
             // accumulators run across units (four chains), added once at the end
-            float chain[4][1][4];
+            float chain[4][MT][4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) chain[q][0][i] = 0.0f;
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) chain[q][mt][i] = 0.0f;
             for (; u + 3 * WK < nun; u += 4 * WK) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    const uint8_t *xr[1] = {xrow + 64 * cpg * (u + q * WK)};
-                    unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * (u + q * WK), g, t, 0, xr, xvalid, cpg,
-                                                      chain[q]);
+                    const uint8_t *xr[MT];
+#pragma unroll
+                    for (int mt = 0; mt < MT; ++mt) xr[mt] = xrow[mt] + 64 * cpg * (u + q * WK);
+                    unit_mma<KIND, false, RB, MT, CPG>(wrow, wrow8, cpg * (u + q * WK), g, t, 0, xr, xvalid, cpg,
+                                                        chain[q]);
                 }
             }
-            for (int q = 0; u < nun; u += WK, ++q) {
-                const uint8_t *xr[1] = {xrow + 64 * cpg * u};
-                unit_mma<KIND, false, RB, 1, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, chain[0]);
+            for (; u < nun; u += WK) {
+                const uint8_t *xr[MT];
+#pragma unroll
+                for (int mt = 0; mt < MT; ++mt) xr[mt] = xrow[mt] + 64 * cpg * u;
+                unit_mma<KIND, false, RB, MT, CPG>(wrow, wrow8, cpg * u, g, t, 0, xr, xvalid, cpg, chain[0]);
             }
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc[j][i] = __float2int_rn((chain[0][0][i] + chain[1][0][i]) + (chain[2][0][i] + chain[3][0][i]));
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[j][mt][i] = __float2int_rn((chain[0][mt][i] + chain[1][mt][i]) +
+                                                   (chain[2][mt][i] + chain[3][mt][i]));
             continue;
         }
         for (; u + 3 * WK < nun; u += 4 * WK) {
-            float part[4][1][4];
+            float part[4][MT][4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) run_unit(u + q * WK, part[q]);
 #pragma unroll
             for (int q = 0; q < 4; ++q) fold(part[q], u + q * WK);
         }
         for (; u < nun; u += WK) {
-            float part[1][4];
+            float part[MT][4];
             run_unit(u, part);
             fold(part, u);
         }
         if constexpr (kInt) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) finish_exact(acc[j][i], f32sum);
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) finish_exact(acc[j][mt][i], f32sum);
         }
     }
     if (!ok) {
@@ -1285,6 +1314,7 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
     }
 
     // ---- 3. combine the K-split warps in index order, then the epilogue.
+    constexpr int kVals = MT * 4;
     uint32_t *red = reinterpret_cast<uint32_t *>(smem + p.red_off);
     if (WK > 1) {
         __syncthreads();  // red may alias the weight tile
@@ -1292,9 +1322,11 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < NRBW; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    red[((((wk - 1) * p.WR + wr) * NRBW + j) * 32 + lane) * 4 + i] =
-                        kInt ? (uint32_t)acc[j][i] : __float_as_uint((float)acc[j][i]);
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        red[((((wk - 1) * p.WR + wr) * NRBW + j) * 32 + lane) * kVals + mt * 4 + i] =
+                            kInt ? (uint32_t)acc[j][mt][i] : __float_as_uint((float)acc[j][mt][i]);
         }
         __syncthreads();
         if (wk != 0) return;
@@ -1302,32 +1334,36 @@ __global__ void __launch_bounds__(512, 2) gemv_stream_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < NRBW; ++j)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t v = red[((((w2 - 1) * p.WR + wr) * NRBW + j) * 32 + lane) * 4 + i];
-                    if constexpr (kInt) acc[j][i] += (int)v;
-                    else acc[j][i] += __uint_as_float(v);
-                }
+                for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t v = red[((((w2 - 1) * p.WR + wr) * NRBW + j) * 32 + lane) * kVals + mt * 4 + i];
+                        if constexpr (kInt) acc[j][mt][i] += (int)v;
+                        else acc[j][mt][i] += __uint_as_float(v);
+                    }
     }
 #pragma unroll
     for (int j = 0; j < NRBW; ++j) {
         const int rb = wr + j * p.WR;
         if (rb >= nrb) break;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (RB == 8 && i >= 2) continue;
-            const int m = 2 * t + (i & 1);
-            const int n = row0 + rb * RB + g + 8 * (i >> 1);
-            if (m >= p.M || n >= p.N) continue;
-            float out;
-            if constexpr (kInt) {
-                const float sw = static_cast<const float *>(p.scale)[n];
-                const float sxm = XQ ? reinterpret_cast<const float *>(smem + p.xq_off)[m] : p.sx[m];
-                out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[j][i]), sxm), sw);
-            } else {
-                out = acc[j][i];
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (RB == 8 && i >= 2) continue;
+                const int m = 8 * mt + 2 * t + (i & 1);
+                const int n = row0 + rb * RB + g + 8 * (i >> 1);
+                if (m >= p.M || n >= p.N) continue;
+                float out;
+                if constexpr (kInt) {
+                    const float sw = static_cast<const float *>(p.scale)[n];
+                    const float sxm = XQ ? reinterpret_cast<const float *>(smem + p.xq_off)[m] : p.sx[m];
+                    out = __fmul_rn(__fmul_rn(__int2float_rn((int)acc[j][mt][i]), sxm), sw);
+                } else {
+                    out = acc[j][mt][i];
+                }
+                p.y[(size_t)m * p.N + n] = out;
             }
-            p.y[(size_t)m * p.N + n] = out;
-        }
     }
 }
 
@@ -1597,11 +1633,11 @@ cudaError_t launch_direct(const GemvParams &p, int S, int threads, int smem, cud
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int KIND, int RB, int CPG, int NRBW, bool XQ = false>
+template <int KIND, int RB, int CPG, int NRBW, bool XQ = false, int MT = 1>
 cudaError_t launch_stream(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    auto *kern = gemv_stream_kernel<KIND, RB, CPG, NRBW, XQ>;
+    auto *kern = gemv_stream_kernel<KIND, RB, CPG, NRBW, XQ, MT>;
     std::call_once(once, [kern] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
@@ -1619,20 +1655,20 @@ cudaError_t launch_stream(const GemvParams &p, int threads, int smem, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int KIND, int RB, int CPG, bool XQ>
+template <int KIND, int RB, int CPG, bool XQ, int MT>
 cudaError_t dispatch_stream_nrbw(const GemvParams &p, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
     switch (nrbw) {
-        case 1: return launch_stream<KIND, RB, CPG, 1, XQ>(p, threads, smem, st, pdl);
-        case 2: return launch_stream<KIND, RB, CPG, 2, XQ>(p, threads, smem, st, pdl);
-        case 3: return launch_stream<KIND, RB, CPG, 3, XQ>(p, threads, smem, st, pdl);
-        default: return launch_stream<KIND, RB, CPG, 4, XQ>(p, threads, smem, st, pdl);
+        case 1: return launch_stream<KIND, RB, CPG, 1, XQ, MT>(p, threads, smem, st, pdl);
+        case 2: return launch_stream<KIND, RB, CPG, 2, XQ, MT>(p, threads, smem, st, pdl);
+        case 3: return launch_stream<KIND, RB, CPG, 3, XQ, MT>(p, threads, smem, st, pdl);
+        default: return launch_stream<KIND, RB, CPG, 4, XQ, MT>(p, threads, smem, st, pdl);
     }
 }
 
-template <int KIND, int CPG, bool XQ = false>
+template <int KIND, int CPG, bool XQ = false, int MT = 1>
 cudaError_t dispatch_stream(const GemvParams &p, int rb, int nrbw, int threads, int smem, cudaStream_t st, bool pdl) {
-    if (rb == 16) return dispatch_stream_nrbw<KIND, 16, CPG, XQ>(p, nrbw, threads, smem, st, pdl);
-    return dispatch_stream_nrbw<KIND, 8, CPG, XQ>(p, nrbw, threads, smem, st, pdl);
+    if (rb == 16) return dispatch_stream_nrbw<KIND, 16, CPG, XQ, MT>(p, nrbw, threads, smem, st, pdl);
+    return dispatch_stream_nrbw<KIND, 8, CPG, XQ, MT>(p, nrbw, threads, smem, st, pdl);
 }
 
 template <bool XQ, int XR>
@@ -1770,8 +1806,12 @@ constexpr int kStreamMinSmem = 80 * 1024;               // dynamic shared memory
 
 // Plans the streaming kernel for a call; false when it does not apply.
 // p must hold the call's geometry, upc = units (no K split) and WK.
-bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out, int &threads, int &smem) {
-    if (a.layout != W4_LAYOUT_ROWMAJOR || a.M > 8 || (a.kind != KIND_W4A16 && a.kind != KIND_W4A8)) return false;
+// MT = 2 (9 to 16 activation rows): one CTA per SM (the staged rows take
+// 2 x 4 KB per 2048 columns), so the cap on shared memory is the SM's.
+bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out, int &threads, int &smem,
+                 int MT = 1) {
+    if (a.layout != W4_LAYOUT_ROWMAJOR || a.M > 8 * MT || (a.kind != KIND_W4A16 && a.kind != KIND_W4A8)) return false;
+    const int cap = MT == 1 ? kStreamSmemPerCta : 220 * 1024;
     if (p.Kb % 16 != 0 || p.upc != p.units) return false;
     const int span_k = p.units * p.unit_k;
     p.wstride = pad_to(p.Kb, 16);
@@ -1782,7 +1822,7 @@ bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out,
     const int fixed = 128 + xbytes + 2 * 128 + (a.xf ? 640 : 0);
     // rows per CTA: the fewest waves of 152 CTAs, rows spread evenly, a whole number of RB-row blocks
     auto rows_for = [&](int RB) -> int {
-        const int rmax = std::min((kStreamSmemPerCta - fixed) / per_row / RB * RB, kStreamMaxBlocks * RB);
+        const int rmax = std::min((cap - fixed) / per_row / RB * RB, kStreamMaxBlocks * RB);
         if (rmax < RB) return 0;
         const int64_t waves = ceil_div(a.N, (int64_t)152 * rmax);
         return (int)std::min<int64_t>(rmax, round_up(ceil_div(a.N, 152 * waves), RB));
@@ -1809,13 +1849,13 @@ bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out,
     p.xq_off = off;
     if (a.xf) off += 640;  // 16 row scales + 16 warps x 8 row maxima (f32)
     // the K-split combine reuses the weight tile once every warp is done with it
-    const int red = (p.WK - 1) * WR * nrbw * 32 * 16;
+    const int red = (p.WK - 1) * WR * nrbw * 32 * 16 * MT;
     p.red_off = p.w_off;
     if (red > R * p.wstride) {
         p.red_off = off;
         off += red;
     }
-    if (off > kStreamSmemPerCta) return false;
+    if (off > cap) return false;
     rb_out = RB;
     nrbw_out = nrbw;
     threads = 32 * WR * p.WK;
@@ -1932,6 +1972,20 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
         if (plan_stream(a, q, rb, nrbw, sthreads, ssmem) && ceil_div(a.N, (int64_t)q.R) >= 120) {
             q.rb = rb;
             return dispatch_q4dp<false>(q, q4dp_threads(q.R), ssmem, st, pdl);
+        }
+    }
+    // Large N, 9 <= M <= 16, no K split, PDL: the streaming kernel with two
+    // activation tiles, one CTA per SM (same arithmetic).
+    if (pdl && (a.kind == KIND_W4A16 || a.kind == KIND_W4A8) && a.M > 8 && S == 1) {
+        GemvParams q = p;
+        int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
+        if (plan_stream(a, q, rb, nrbw, sthreads, ssmem, 2) && ceil_div(a.N, (int64_t)q.R) >= 120) {
+            if (a.kind == KIND_W4A8) return dispatch_stream<KIND_W4A8, 1, false, 2>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+            switch (p.cpg) {
+                case 1: return dispatch_stream<KIND_W4A16, 1, false, 2>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+                case 4: return dispatch_stream<KIND_W4A16, 4, false, 2>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+                default: return dispatch_stream<KIND_W4A16, 0, false, 2>(q, rb, nrbw, sthreads, ssmem, st, pdl);
+            }
         }
     }
     // Large N, M <= 8, no K split, PDL: the streaming kernel (same arithmetic).
