@@ -34,6 +34,13 @@
 //    bulk copy per 64-channel block and transposed in shared memory (4x4
 //    byte transposes with PRMT) into the row-major tile; from there the
 //    arithmetic is the row-major path's, so the two layouts agree bit for bit.
+//  * Under PDL, large-N calls stream instead (gemv_stream_kernel): one CTA
+//    per ~N/152 rows, its whole weight range requested by bulk copies at
+//    entry, at most two CTAs per SM so the next launch prefetches while this
+//    one computes -- the same arithmetic, so the same bits.  W4A8 at M = 1
+//    uses integer dot products there (gemv_q4dp_kernel), and the fused
+//    quantize + linear call quantises the activation row inside these
+//    kernels (stage_x_q8).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -944,21 +951,6 @@ __global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant_
 
 // ---------------------------------------------------------------- fused Q8 quantisation
 
-// Q8 code of v for scale sx > 0 (quantize_row_q8: clamp(rint(fl(v / sx)), -127, 127)),
-// given r = fl(1 / sx) (finite).  t = fl(v * r) is within 2^-16 + 2^-24 of
-// x = v / sx when |x| < 256 (two correctly rounded operations, each within
-// 2^-24 relative), and fl(x) within ulp(x) / 2 <= 2^-17 of x, so t and fl(x)
-// lie within 2^-15 of each other.  When t is farther than 2^-13 from every
-// half-integer, rint(t) == rint(fl(x)); otherwise the IEEE quotient itself
-// is rounded.
-W4_DEV int q8_code_fast(float v, float sx, float r) {
-    const float t = __fmul_rn(v, r);
-    const float rt = rintf(t);
-    int q;
-    if (fabsf(t) < 256.0f && 0.5f - fabsf(t - rt) > 0x1p-13f) q = __float2int_rn(rt);
-    else q = __float2int_rn(__fdiv_rn(v, sx));
-    return min(max(q, -127), 127);
-}
 
 // W4A8 activations straight from f32 ("Q4 weights x Q8 activations"): every
 // CTA quantises the M <= 8 rows itself with quantize_row_q8's arithmetic
@@ -1052,9 +1044,13 @@ W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
     }
     __syncthreads();
     if (regs) {
-        // codes by t = fl(v * fl(1 / sx)) (see q8_code_fast); values whose t
-        // lies within 2^-13 of a half-integer (or all, when 1 / sx overflows)
-        // are redone with the IEEE quotient
+        // Codes clamp(rint(fl(v / sx)), -127, 127) by t = fl(v * r), r = fl(1 / sx)
+        // finite: t is within 2^-16 + 2^-24 of x = v / sx when |x| < 256 (two
+        // correctly rounded operations, each within 2^-24 relative) and fl(x)
+        // within ulp(x) / 2 <= 2^-17 of x, so t and fl(x) lie within 2^-15 of
+        // each other; when t is farther than 2^-13 from every half-integer,
+        // rint(t) == rint(fl(x)).  The other values (or all, when 1 / sx
+        // overflows) are redone with the IEEE quotient.
         const float sx = sx_s[0];
         const float r = sx != 0.0f ? __frcp_rn(sx) : 0.0f;
         const bool fast = isfinite(r);
