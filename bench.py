@@ -792,7 +792,7 @@ class Microdecoder:
         self.chain_ws = torch.zeros(ops.chain_workspace_bytes(self.desc[0], 1024), dtype=torch.uint8, device="cuda")
         torch.cuda.synchronize()
 
-    launches_per_frame = {"per_call": 1 + 15 * 5 * 11, "chain": 1}
+    launches_per_frame = {"per_call": 1 + 15 * 5 * 11, "per_call_fused": 15 * 5 * 7, "chain": 1}
 
     def descriptors(self, c: int):
         """(w, sw, y, input) per linear of weight set c, in the frame's dataflow order."""
@@ -834,13 +834,39 @@ class Microdecoder:
 
         return microdecoder_frame_ops(linear, quant, layers, self.synth.MICRODECODER_PASSES, self.x0)
 
+    def frame_fused(self, i: int = 0):
+        """The frame call by call with w4_linear_q4_f32: every linear takes the
+        f32 output before it and quantises it itself (one launch per linear)."""
+        ops = self.ops
+        layers = self.sets[i % len(self.sets)]
+        scratch = {1024: self.sites[0], 3072: self.sites[3]}
+
+        def linear(li, name, x):
+            pk, sw, K = layers[li][name]
+            q, s = scratch[K]
+            return ops.linear_q4_f32(x, pk, sw, K=K, flags=ops.FLAG_PDL, out=self.y[name], xq=q, sx=s)[0]
+
+        h = self.x0
+        y = None
+        for _ in range(self.synth.MICRODECODER_PASSES):
+            for li in range(len(layers)):
+                linear(li, "q", h)
+                linear(li, "k", h)
+                v = linear(li, "v", h)
+                o = linear(li, "o", v)
+                linear(li, "gate", o)
+                u = linear(li, "up", o)
+                y = linear(li, "down", u)
+                h = y
+        return y
+
 
 def time_microdecoder(copies: int, frames: int, warmup: int, mode: str = "chain"):
     """Exactly `frames` frames replayed from one CUDA graph per weight set;
     returns (ms_per_frame, t0, t1)."""
     import torch
     md = Microdecoder(copies)
-    run = md.frame_chain if mode == "chain" else md.frame
+    run = {"chain": md.frame_chain, "per_call_fused": md.frame_fused}.get(mode, md.frame)
     st = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(st):
@@ -938,16 +964,17 @@ def time_oracle_microdecoder(seconds: float, openmp: bool = True):
 
 
 def microdecoder_line(l2: int, peak_gbs: float, frames: int, warmup: int):
-    """Frame time and effective weight GB/s of the one-kernel chain path and
-    of the per-call path (826 launches), each L2-resident (one weight set,
-    the cache residency that motivates int4 here) and with rotating weight
-    sets larger than L2."""
+    """Frame time and effective weight GB/s of the one-kernel chain path, of
+    the per-call path (quantize_row_q8 + linear_q4: 826 launches) and of the
+    per-call path through w4_linear_q4_f32 (525 launches), each L2-resident
+    (one weight set, the cache residency that motivates int4 here) and with
+    rotating weight sets larger than L2."""
     from w4a16_int4_quantized_gb300 import synth
     wbytes = microdecoder_weight_bytes()
     per_frame = wbytes * synth.MICRODECODER_PASSES
     rot = max(2, int(np.ceil(2.2 * l2 / wbytes)))
     out = {}
-    for mode in ("chain", "per_call"):
+    for mode in ("chain", "per_call", "per_call_fused"):
         for label, copies in (("rotating", rot), ("l2_resident", 1)):
             ms, t0, t1 = time_microdecoder(copies, frames, warmup, mode)
             out[f"{mode}_{label}"] = {"ms_per_frame": round(ms, 4), "frames_per_s": round(1e3 / ms, 1),
