@@ -300,11 +300,11 @@ def time_oracle(w, seconds: float, openmp: bool = True):
         call = lambda: o.linear_q4_group(xq, sx, wp, s, z, w["K"], w["G"])
         what = "ref_linear_q4_group"
     else:
+        # the step: quantize_row_q8 of the activations, then linear_q4
         x, W = oracle_inputs(w)
-        xq, sx, _ = o.quantize_row_q8(x)
         wp, sw = o.quantize_matrix_q4(W)
-        call = lambda: o.linear_q4(xq, sx, wp, sw, w["K"])
-        what = "ref_linear_q4"
+        call = lambda: o.linear_q4(*o.quantize_row_q8(x)[:2], wp, sw, w["K"])
+        what = "ref_quantize_row_q8 + ref_linear_q4"
     call()
     n, t0 = 0, time.perf_counter()
     while True:
