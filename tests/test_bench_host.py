@@ -1,0 +1,43 @@
+"""Host-side pieces of bench.py (no GPU): every workload's byte and op counts,
+metric names and the reference arm's JSON line on a tiny sample."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+@pytest.mark.parametrize("name", sorted(bench.WORKLOADS))
+def test_workload_counts(name):
+    w = bench.WORKLOADS[name]
+    wb, sb = bench.weight_bytes(w), bench.step_bytes(w)
+    assert 0 < wb < sb
+    kp = w["K"] + (w["K"] & 1)
+    packed = w["N"] * (w["K"] if w["kind"] == "w8a16" else kp // 2)
+    assert wb >= packed
+    assert bench.step_ops(w) == 2 * w["M"] * w["N"] * w["K"]
+    value, unit = bench.metric_of(w, 1.0)
+    assert value > 0 and unit in ("GB/s", "TOPS", "TFLOP/s")
+    assert ("decode" in bench.metric_name(w)) == (w["regime"] == "decode")
+
+
+def test_default_workload_bytes():
+    """The default line's algorithmic bytes: weights + f16 scales + bf16 x + f32 y."""
+    w = bench.WORKLOADS["w4a16_gemv_m1"]
+    assert bench.step_bytes(w) == 2048 * 1024 + 2048 * 64 * 2 + 2048 * 2 + 2048 * 4
+
+
+def test_reference_arm_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "0", "--cpu-seconds", "0.5"], capture_output=True, text=True, timeout=600,
+                         cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
