@@ -74,7 +74,11 @@ enum {
      * the weights and scales, while the previous kernel on `stream` is still
      * running; it waits for that kernel before it reads x or writes y.  Only
      * set it when no earlier work on the stream that may still be running
-     * writes the weight or scale buffers of this call. */
+     * writes the weight or scale buffers of this call.  The library's kernels
+     * let the next kernel on the stream start early, as PDL allows: a kernel
+     * of the caller's launched after them with programmatic stream
+     * serialization must execute griddepcontrol.wait before it reads their
+     * outputs (the CUDA rule for any such kernel). */
     W4_FLAG_PDL = 1u
 };
 
