@@ -394,7 +394,7 @@ class Workload:
             return 1
         if w["kind"] == "w8a16":
             return 1 + (1 if self.ws is not None else 0)  # (f32 -> bf16 prepass), linear
-        if w["kind"] == "w4a8" and w["M"] <= 8 and w["layout"] == 0 and w["N"] >= 1024:
+        if w["kind"] == "w4a8" and w["M"] == 1 and w["layout"] == 0 and w["N"] >= 1024:
             return 1  # the rows are quantised inside the linear
         return 2 + (1 if self.ws is not None else 0)  # quantize, (int8 -> f16 prepass), linear
 
@@ -420,7 +420,7 @@ class Workload:
     def step(self, i: int, flags: int = 1):
         w = self.w
         if w["kind"] == "w4a8":
-            # quantize_row_q8 + linear_q4 as one library call (fused for M <= 8)
+            # quantize_row_q8 + linear_q4 as one library call (one kernel at M = 1)
             c = i % self.copies
             self.ops.linear_q4_f32(self.xf[c], self.wt[c], self.s[c], K=w["K"], N=w["N"], layout=w["layout"],
                                    flags=flags, out=self.y[c], xq=self.x[c], sx=self.sx[c], workspace=self.ws)

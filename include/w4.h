@@ -151,9 +151,9 @@ w4_status w4_linear_q4(const int8_t *xq, const float *sx, const uint8_t *w, cons
  * ftts_kernels::int4 and ::int8: activations are quantised per row before
  * the W4A8 linear).  x [M][K] f32 device; xq [M][K] int8 and sx [M] f32
  * receive exactly what w4_quantize_row_q8 writes; y [M][N] what
- * w4_linear_q4 writes for them -- bit for bit.  For M <= 8 on the row-major
+ * w4_linear_q4 writes for them -- bit for bit.  For M = 1 on the row-major
  * layout with N >= 1024 the quantisation runs inside the linear (every
- * thread block quantises the rows it needs; one launch); otherwise the two
+ * thread block quantises the row itself; one launch); otherwise the two
  * kernels run in order.  Other arguments, limits and errors: those of
  * w4_linear_q4 and w4_quantize_row_q8. */
 w4_status w4_linear_q4_f32(const float *x, const uint8_t *w, const float *sw, float *y, int8_t *xq, float *sx,

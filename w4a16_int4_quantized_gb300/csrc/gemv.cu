@@ -1932,13 +1932,16 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
         if (a.M >= 4)
             while (s.WR < 4 && a.N / (s.RB * s.WR * 2) >= 2 * 152) s.WR *= 2;
     }
-    // Fused W4A8 (f32 activations quantised in every CTA): the streaming
-    // kernel when it applies, else the row quantizer and then this path.
+    // Fused W4A8 (f32 activations quantised in every CTA, M = 1): the
+    // streaming kernels when they apply, else the row quantizer and then
+    // this path.
     if (a.xf) {
         GemvParams q = p;
         q.WK = s.WK;
         int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
-        if (a.kind == KIND_W4A8 && S == 1 && plan_stream(a, q, rb, nrbw, sthreads, ssmem) &&
+        // M = 1 only: more rows take the per-element quantiser path, slower
+        // inside every CTA than the separate quantizer kernel
+        if (a.kind == KIND_W4A8 && a.M == 1 && S == 1 && plan_stream(a, q, rb, nrbw, sthreads, ssmem) &&
             ceil_div(a.N, (int64_t)q.R) >= 120) {
             q.xf = a.xf;
             q.xq_out = a.xq_out;
