@@ -190,3 +190,40 @@ def test_linear_q4_f32_validation(lib):
     assert f(xq=None) == lib.W4_EINVAL
     assert f(M=0) == lib.W4_OK
     assert f(M=-1) == lib.W4_EINVAL
+
+
+def test_workspace_bytes_formula(lib):
+    """Scratch of the tensor-core GEMM: the f16 image of the int8 / f32
+    activations, M * round_up(K, 8) * 2 bytes for M > 16; none for W4A16 or
+    the decode kernels."""
+    r = lib.raw
+    ops = lib
+    for op in (ops.OP_LINEAR_Q4, ops.OP_LINEAR_Q8, ops.OP_LINEAR_Q4_GROUP, ops.OP_LINEAR_W8A16):
+        assert r.w4_workspace_bytes(op, 16, 2048, 2048, 128) == 0
+        assert r.w4_workspace_bytes(op, 17, 2048, 2048, 128) == 17 * 2048 * 2
+        assert r.w4_workspace_bytes(op, 2048, 13312, 2047, 128) == 2048 * 2048 * 2
+        assert r.w4_workspace_bytes(op, 32, 64, 100, 4) == 32 * 104 * 2
+        assert r.w4_workspace_bytes(op, 32, 0, 100, 4) == 0
+        assert r.w4_workspace_bytes(op, 32, 64, 0, 4) == 0
+    assert r.w4_workspace_bytes(ops.OP_LINEAR_W4A16, 2048, 13312, 2048, 128) == 0
+    assert r.w4_workspace_bytes(99, 2048, 13312, 2048, 128) == 0
+
+
+def test_noalloc_validation(lib):
+    r = lib.raw
+    f = lambda M=1, N=8, K=64, layout=0: r.w4_linear_q4_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, M, N, K, layout, None)
+    assert f(M=4096, K=2048) == lib.W4_ESHAPE      # 16 MiB of scratch > the fixed 8 MiB
+    assert f(layout=3) == lib.W4_EINVAL
+    assert f(K=2_000_000) == lib.W4_ESHAPE
+    assert f(M=-1) == lib.W4_EINVAL
+    assert f(M=0) == lib.W4_OK
+
+
+def test_probe_and_version(lib):
+    r = lib.raw
+    v = C.c_double(0.0)
+    assert r.w4_probe_mma_peak(2, FAKE, 1 << 20, C.byref(v), None) == lib.W4_EINVAL   # unknown kind
+    assert r.w4_probe_mma_peak(0, None, 1 << 20, C.byref(v), None) == lib.W4_EINVAL   # no scratch
+    assert r.w4_probe_mma_peak(1, FAKE, 1 << 20, None, None) == lib.W4_EINVAL        # no result pointer
+    ver = r.w4_version()
+    assert ver >= 100 and ver // 10000 < 100
