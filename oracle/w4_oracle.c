@@ -35,6 +35,10 @@
  *   23 activation bf16 decoded as f16
  *   24 grouped W4A8 zero point indexed by group only
  *   25 grouped W4A8 zero points ignored (the constant 8 used)
+ *   26 Q8 weight matrix quantised with 128 in place of 127
+ *   27 Q8 weight matrix row n quantised from row n - 1
+ *   28 bf16 prefill dequantisation rounded through f16 instead
+ *   29 bf16 prefill dequantisation truncated instead of rounded to even
  * (s11, the missing NULL check, would crash the test process and is covered
  * by the host-side validation tests of the CUDA library instead.)
  */
@@ -220,7 +224,15 @@ int ref_quantize_matrix_q8(const float *W, int64_t N, int64_t K, int8_t *q, floa
     if (N < 0 || K < 0) return REF_EINVAL;
     if (N == 0) return REF_OK;
     if (!sw || (K > 0 && (!W || !q))) return REF_EINVAL;
-    for (int64_t n = 0; n < N; ++n) ref_quantize_row(W + n * K, K, 127, q + n * K, &sw[n]);
+    for (int64_t n = 0; n < N; ++n) {
+#if MUT(26)
+        ref_quantize_row(W + n * K, K, 128, q + n * K, &sw[n]);
+#elif MUT(27)
+        ref_quantize_row(W + (n > 0 ? n - 1 : 0) * K, K, 127, q + n * K, &sw[n]);
+#else
+        ref_quantize_row(W + n * K, K, 127, q + n * K, &sw[n]);
+#endif
+    }
     return REF_OK;
 }
 
@@ -603,6 +615,20 @@ int ref_linear_w4a16_lanes(const uint16_t *x, const uint8_t *w, const uint16_t *
     return REF_OK;
 }
 
+#if MUT(28)
+/* Planted mistake only: f32 -> binary16, round to nearest even (normals;
+ * the products used here never underflow binary16's normal range). */
+static uint16_t f32_to_f16_rne_mutant(float f) {
+    if (f == 0.0f) return 0;
+    int e;
+    const double m = frexp(fabs((double)f), &e); /* |f| = m * 2^e, m in [0.5, 1) */
+    double r = rint(ldexp(m, 11));               /* 11 significant bits */
+    if (r == 2048.0) { r = 1024.0; ++e; }
+    const unsigned bits = (unsigned)((e - 1 + 15) << 10) | ((unsigned)r - 1024u);
+    return (uint16_t)(bits | (f < 0 ? 0x8000u : 0u));
+}
+#endif
+
 /* The prefill reading: each weight dequantized once to bf16,
  * w = bf16_rne(f32(q) * f32(s)) (the product is exact in f32), then summed
  * against x in double. */
@@ -618,7 +644,15 @@ int ref_linear_w4a16_bf16dequant(const uint16_t *x, const uint8_t *w, const uint
             for (int64_t k = 0; k < K; ++k) {
                 const float sg = (float)scale_of(s, n, ng, k / G);
                 const float wq = (float)ref_nibble_signed(nib(row, k)) * sg;
+#if MUT(28)
+                const float wb = ref_f16_to_f32(f32_to_f16_rne_mutant(wq));
+#elif MUT(29)
+                uint32_t wu;
+                memcpy(&wu, &wq, sizeof wu);
+                const float wb = ref_bf16_to_f32((uint16_t)(wu >> 16));
+#else
                 const float wb = ref_bf16_to_f32(ref_f32_to_bf16_rne(wq));
+#endif
                 acc += (double)act_bf16(x[m * K + k]) * (double)wb;
             }
             y64[m * N + n] = acc;

@@ -302,6 +302,54 @@ def pin_dequant_then_matmul_w4a16(o):
         assert np.all(np.abs(yb - ref) <= 2.0 ** -8 * scale + 1e-6), (M, N, K, G)
 
 
+def pin_quantize_matrix_q8(o):
+    # [int8] summary: the weight matrix is quantised row by row with the
+    # activation recipe (scale = max|row| / 127, ties to even, [-127, 127]).
+    # Hand row: max 127 gives s = 1 exactly, so the codes are rint(v).
+    W = np.array([[127.0, 0.5, 1.5, 2.5, -2.5, 126.5],
+                  [-254.0, 1.0, 3.0, -5.0, 127.0, 0.0]], np.float32)
+    q, sw = o.quantize_matrix_q8(W)
+    assert list(sw) == [1.0, 2.0], sw
+    assert q[0].tolist() == [127, 0, 2, 2, -2, 126], q[0]
+    assert q[1].tolist() == [-127, 0, 2, -2, 64, 0], q[1]   # 1.5 -> 2, 2.5 -> 2, 63.5 -> 64
+    for K in (1, 37, 300):
+        W = synth.weights_f32(900 + K, 7, K)
+        W[3] *= 50.0                                   # rows on different scales
+        W[5, K // 2] = -4.0 * float(np.abs(W[5]).max())  # a negative extreme
+        q, sw = o.quantize_matrix_q8(W)
+        qi = q.astype(np.int64)
+        assert qi.min() >= -127 and np.all(np.abs(qi).max(axis=1) == 127), "codes in [-127, 127], the extreme at 127"
+        amax = np.abs(W.astype(np.float64)).max(axis=1)
+        assert np.all(np.abs(sw.astype(np.float64) * 127 - amax) <= 2.0 ** -23 * amax * 127)
+        err = np.abs(W.astype(np.float64) - qi * sw[:, None].astype(np.float64))
+        assert np.all(err <= 0.5 * sw[:, None] * (1 + 1e-6)), "nearest code per row"
+        qn, swn = o.quantize_matrix_q8(-W)
+        assert np.array_equal(sw, swn) and np.array_equal(qi, -qn.astype(np.int64)), "negation symmetry"
+    assert not o.quantize_matrix_q8(np.zeros((2, 8), np.float32))[0].any()
+
+
+def pin_bf16_dequant_one_hot(o):
+    # One-hot activations make y[m, n] the dequantised weight w[n, m] itself:
+    # bf16_rne(q * s), q * s exact in f32; compared with torch's bf16 rounding.
+    import torch
+    K, N, G = 64, 24, 32
+    _, w, s = synth.w4a16_inputs(950, 1, N, K, G)
+    s = s.copy()
+    s[0, 0] = 0x3C0C          # 1 + 3 * 2^-8: q = 2 gives an exact bf16 tie
+    s[1, 0] = 0x3C03          # 1 + 3 * 2^-10
+    q = np_unpack_codes(w, K, biased=False)
+    q[0, :] = 2
+    q[1, :] = np.arange(K) % 16 - 8
+    w = np_pack(q & 0xF, 0)
+    eye = np.zeros((K, K), np.uint16)
+    eye[np.arange(K), np.arange(K)] = 0x3F80   # bf16 1.0
+    y = o.linear_w4a16_bf16dequant(eye, w, s, K, G)
+    prod = (q.astype(np.float64) * np_f16(s)[:, np.arange(K) // G]).astype(np.float32)
+    want = torch.from_numpy(prod).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(y.T, want), np.argwhere(y.T != want)[:4]
+    assert want[0, 0] == 2.0 * (1 + 2.0 ** -6), "the tie rounds to even (up here)"
+
+
 def pin_interleave_index_pattern(o):
     """Pack index patterns and read back where each nibble landed
     ("The weight layout, measured").  Two patterns together identify the
