@@ -96,10 +96,11 @@ WORKLOADS = {
 
 
 # DRAM bytes (read + write) per launch of the roofline's kernel from one ncu
-# capture (profiles/); None where no capture matches the current kernel.
+# capture of that kernel on that workload; None where no capture matches the
+# current kernel.
 TRAFFIC = {
-    "w4a16_gemv_m1": 2393856,                 # profiles/gemv_w4a16_m1_n2048_k2048.md
-    "w4a8_gemv_m1": 2141184,                  # profiles/gemv_w4a8_fused_m1_n2048_k2048.md
+    "w4a16_gemv_m1": 2393856,                 # streaming W4A16 GEMV, M=1, N=K=2048, G=32
+    "w4a8_gemv_m1": 2141184,                  # fused quantize + W4A8 dp4a GEMV, M=1, N=K=2048
 }
 
 

@@ -321,7 +321,8 @@ w4_status w4_pack_block32(const uint8_t *w_rowmajor, const uint16_t *scales_f16,
 
 /* ---- host queries ---------------------------------------------------------- */
 
-/* Bytes of device scratch the op needs at this shape (0: pass NULL). */
+/* Bytes of device scratch the op needs at this shape (0: pass NULL).
+ * SIZE_MAX when M, N or K is 2^31 or more (no call accepts such a shape). */
 size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G);
 
 /* Reads (and when clear != 0, clears) the device status word of the

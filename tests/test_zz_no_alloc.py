@@ -3,8 +3,8 @@ device memory while they run (a serving process with a memory budget fixed
 at start-up, a host framework whose allocator owns the device, a loop where
 an allocation could block).  Large batches use a fixed scratch array inside
 the library instead of caller workspace; the result must be the same as
-w4_linear_q4's, bit for bit (the W4A8 bar), on consecutive calls that reuse
-that array with different shapes.
+w4_linear_q4's and the CPU oracle's, bit for bit (the W4A8 bar), on
+consecutive calls that reuse that array with different shapes.
 
 This file is collected last on purpose, and passes alone in a fresh process
 as well as after the rest of the suite.
@@ -68,6 +68,10 @@ def test_noalloc_matches_linear_q4_on_consecutive_calls(ops):
         want = _reference(ops, xq, sx, w, sw, M, N, K)
         torch.cuda.synchronize()
         assert torch.equal(got.view(torch.int32), want.view(torch.int32)), (M, N, K)
+        # and directly against the CPU oracle's linear_q4 on the same codes
+        import oracle
+        ref = oracle.get().linear_q4(xq.cpu().numpy(), sx.cpu().numpy(), w.cpu().numpy(), sw.cpu().numpy(), K)
+        assert np.array_equal(got.cpu().numpy().view(np.int32), ref.view(np.int32)), (M, N, K)
     assert ops.device_status() == 0
 
 

@@ -96,6 +96,10 @@ w4_status check_workspace(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G
 
 }  // namespace
 
+namespace w4 {
+w4_status record_cuda_error(cudaError_t e) { return cuda_status(e); }
+}  // namespace w4
+
 extern "C" {
 
 w4_status w4_quantize_row_q8(const float *x, int64_t M, int64_t K, int8_t *q, float *sx, int32_t *rowsum,
@@ -323,6 +327,7 @@ size_t w4_chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32
 
 size_t w4_workspace_bytes(int32_t op, int64_t M, int64_t N, int64_t K, int64_t G) {
     if (M <= 16 || N <= 0 || K <= 0) return 0;
+    if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return SIZE_MAX;  // beyond every call's limits
     switch (op) {
         case W4_OP_LINEAR_Q4: return w4::gemm_workspace_bytes(w4::KIND_W4A8, M, N, K, G);
         case W4_OP_LINEAR_Q8: return w4::gemm_workspace_bytes(w4::KIND_W8A8, M, N, K, G);

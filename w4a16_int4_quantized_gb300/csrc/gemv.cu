@@ -952,8 +952,10 @@ __global__ void __launch_bounds__(512) gemv_direct_kernel(const __grid_constant_
 // ---------------------------------------------------------------- fused Q8 quantisation
 
 
-// W4A8 activations straight from f32 ("Q4 weights x Q8 activations"): every
-// CTA quantises the M <= 8 rows itself with quantize_row_q8's arithmetic
+// W4A8 activations straight from f32 ("Q4 weights x Q8 activations"): at
+// M = 1 (the only case the host routes here; more rows run the separate
+// quantizer kernel first) every CTA quantises the row itself with
+// quantize_row_q8's arithmetic
 // (amax over the row, sx = fl(amax / 127), codes clamp(rint(fl(v / sx)))),
 // and stages the codes as stage_x<KIND_W4A8> would (biased f16 pairs), the
 // row scales in shared memory.  CTA 0 also writes the codes and scales out.
@@ -1150,7 +1152,7 @@ W4_DEV void stage_x_q8(const GemvParams &p, int nthr, uint8_t *smem) {
 template <int KIND, int RB, int CPG, int NRBW, bool XQ, int MT = 1>
 __global__ void __launch_bounds__(512, MT == 1 ? 2 : 1) gemv_stream_kernel(const __grid_constant__ GemvParams p) {
     static_assert(KIND == KIND_W4A16 || KIND == KIND_W4A8, "row-major int4 kinds");
-    static_assert(!XQ || (KIND == KIND_W4A8 && MT == 1), "fused quantisation is W4A8's, M <= 8");
+    static_assert(!XQ || (KIND == KIND_W4A8 && MT == 1), "fused quantisation is W4A8's, one activation tile (the host uses it at M = 1)");
     griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr bool kInt = kIntAcc<KIND>;

@@ -37,6 +37,9 @@ struct LinearArgs {
     float *sx_out;
 };
 
+// capi.cu -- W4_OK for cudaSuccess; otherwise records e for w4_last_cuda_error and returns W4_ECUDA.
+w4_status record_cuda_error(cudaError_t e);
+
 // tmap.cu -- TMA tensor map of a tiled box (rank <= 5); strides of dims 1..rank-1 in bytes.
 bool encode_tmap(CUtensorMap *map, CUtensorMapDataType type, int rank, const void *base, const uint64_t *dims,
                  const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);

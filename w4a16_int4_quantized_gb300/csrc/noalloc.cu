@@ -21,6 +21,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "internal.h"
 #include "w4.h"
 
 namespace {
@@ -54,13 +55,21 @@ cudaError_t scratch_address(void **out) {
 
 extern "C" w4_status w4_linear_q4_noalloc(const int8_t *xq, const float *sx, const uint8_t *w, const float *sw,
                                           float *y, int64_t M, int64_t N, int64_t K, int32_t layout, void *stream) {
+    // w4_linear_q4's own argument checks come first, so an invalid call gets
+    // the same error from both entry points; the scratch size is computed
+    // only for arguments inside those limits.
     if (M < 0 || N < 0 || K < 0) return W4_EINVAL;
+    if (layout != W4_LAYOUT_ROWMAJOR && layout != W4_LAYOUT_N64) return W4_EINVAL;
+    if (K > 1000000 || M >= ((int64_t)1 << 31) || N >= ((int64_t)1 << 31)) return W4_ESHAPE;
+    if (layout == W4_LAYOUT_N64 && N % 64) return W4_ESHAPE;
+    if (M == 0 || N == 0) return W4_OK;
+    if (!y || !sx || !sw || (K > 0 && (!xq || !w))) return W4_EINVAL;
     const size_t need = w4_workspace_bytes(W4_OP_LINEAR_Q4, M, N, K, 0);
     if (need > (size_t)W4_NOALLOC_SCRATCH_BYTES) return W4_ESHAPE;  // batch too large for the fixed scratch
     void *scratch = nullptr;
     if (need > 0) {
         const cudaError_t e = scratch_address(&scratch);
-        if (e != cudaSuccess) return W4_ECUDA;
+        if (e != cudaSuccess) return w4::record_cuda_error(e);
     }
     // The prepass writes every byte of the scratch it uses (zero padding
     // included) before the GEMM reads it, so nothing has to start at zero.
