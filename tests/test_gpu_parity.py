@@ -271,7 +271,8 @@ def test_w4a16_batch_invariance(ops, N, K, G):
 
 @pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
 @pytest.mark.parametrize("N,K,G", [(2048, 2048, 32), (2048, 2047, 32), (13312, 2048, 128), (1024, 1024, 128),
-                                   (3072, 2048, 128), (4096, 8192, 128), (1000, 4096, 32)])
+                                   (3072, 2048, 128), (4096, 8192, 128), (1000, 4096, 32), (1100, 1024, 64),
+                                   (5000, 2048, 32), (2056, 512, 128), (3000, 1022, 2)])
 def test_w4a16_pdl_same_bits(ops, ora, M, N, K, G):
     """With W4_FLAG_PDL, large-N decode calls stream whole-SM row ranges with
     bulk copies (a different kernel); the arithmetic, and so every bit, is the

@@ -105,6 +105,22 @@ W4_DEV void tma_load_3d(void *dst, const void *map, int c0, int c1, int c2, uint
         : "memory");
 }
 
+// Bulk prefetch of [src, src + bytes) from global memory into L2 (a hint:
+// nothing is written to shared memory).  src 16-byte aligned, bytes a
+// multiple of 16.
+W4_DEV void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// 16 bytes from global memory through L2 only (not cached in L1).
+W4_DEV uint4 ldg_cg_u128(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 // ---------------------------------------------------------------- PDL
 
 W4_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

@@ -111,6 +111,8 @@ struct GemvParams {
     int rb;           // streaming kernels: rows per mbarrier block
     int x_vec;       // activation rows can be read with aligned vector loads
     int s_vec;       // scale rows can be read as 16-byte vectors
+    int x_al;        // the activation base is 16-byte aligned
+    int x_pref;      // bytes of the activation row prefetched into L2 before the PDL wait (0: none)
 };
 
 // ---------------------------------------------------------------- MMA wrappers
@@ -127,14 +129,14 @@ W4_DEV void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint3
 // 0x4300 | v is the bf16 128 + v (v < 128); with v = u ^ 8 = q + 8 the value
 // is 136 + q, and subtracting 136 is exact.
 W4_DEV void unpack_signed_bf16(uint32_t w, uint32_t (&p)[4]) {
-    const __nv_bfloat162 off = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)0x4308),
-                                                  __ushort_as_bfloat16((unsigned short)0x4308));
+    // one shift, one LOP3 ((v & 0x000F000F) ^ 0x43084308) and one bf16x2
+    // subtraction per pair, written out so nothing else is generated around them
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) ^ 0x43084308u;
-        __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162 *>(&v);
-        h = __hsub2(h, off);
-        p[i] = *reinterpret_cast<const uint32_t *>(&h);
+        uint32_t v = w, r;
+        if (i > 0) asm("shr.b32 %0, %1, %2;" : "=r"(v) : "r"(w), "r"(4 * i));
+        asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x43084308u));
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(p[i]) : "r"(r), "r"(0x43084308u));
     }
 }
 
@@ -142,13 +144,13 @@ W4_DEV void unpack_signed_bf16(uint32_t w, uint32_t (&p)[4]) {
 // integers q: P0 = (k0, k4), P1 = (k1, k5), P2 = (k2, k6), P3 = (k3, k7).
 // 0x6400 | u is the f16 1024 + u; subtracting 1032 is exact.
 W4_DEV void unpack_biased_f16(uint32_t w, uint32_t (&p)[4]) {
-    const __half2 off = __halves2half2(__ushort_as_half((unsigned short)0x6408), __ushort_as_half((unsigned short)0x6408));
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const uint32_t v = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-        __half2 h = *reinterpret_cast<const __half2 *>(&v);
-        h = __hsub2(h, off);
-        p[i] = *reinterpret_cast<const uint32_t *>(&h);
+        uint32_t v = w, r;
+        if (i > 0) asm("shr.b32 %0, %1, %2;" : "=r"(v) : "r"(w), "r"(4 * i));
+        // (v & 0x000F000F) | 0x64006400
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(v), "r"(0x000F000Fu), "r"(0x64006400u));
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(p[i]) : "r"(r), "r"(0x64086408u));
     }
 }
 
@@ -1478,6 +1480,216 @@ __global__ void __launch_bounds__(512, 2) gemv_q4dp_kernel(const __grid_constant
     }
 }
 
+// ---------------------------------------------------------------- W4A16, one activation row
+//
+// linear_w4a16_group at M = 1 (the decode step of "Fused int4 and int8
+// dequantize-matmul in C", section 4): the streaming kernel's data movement
+// -- each CTA's weight rows and f16 scale rows requested by bulk copies at
+// entry, before griddepcontrol.wait, with the PDL trigger at entry -- but
+// all 16 warps of the CTA at work once the wait returns, and no staging of
+// the activations in shared memory:
+//  * the activation row (asked into L2 before the wait) arrives in shared
+//    memory by one bulk copy issued right after the wait -- a few line
+//    requests per CTA instead of one per thread on the same 4 KB;
+//  * warp w takes the units (groups) u = w, w + 16, ...; its lanes 0-3 turn
+//    the activations of those units into the MMA's B fragments, in the pair
+//    order of the unpacked nibbles;
+//  * for every 16-row block the warp forms each unit's partial with the
+//    streaming kernel's MMA sequence (the same k-slot order, the chunks of
+//    the unit in order, from a zero accumulator), so each partial has the
+//    same bits, and stores it to shared memory;
+//  * after one barrier, thread (row, w') of the WK K-warps of the other M <= 16
+//    paths folds its units u = w', w' + WK, ... in order, acc = fma(s_u,
+//    part_u, acc), and the WK sums are added in index order -- bit for bit
+//    the result of every other M <= 16 path for the same (N, K, G).
+template <int CPG, int NU, int JJ>
+__global__ void __launch_bounds__(512, 2) gemv_m1_w4a16_kernel(const __grid_constant__ GemvParams p) {
+    griddep_launch_dependents();
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int NCH = NU * CPG;  // 32-column chunks per warp: NU units of CPG chunks
+    constexpr int WK = 4;          // K-warp chains of the other M <= 16 paths
+    constexpr bool kPre = NCH <= 4;  // the first row block unpacked before the wait
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int row0 = blockIdx.x * p.R;
+    const int rows = min(p.R, p.N - row0);
+    const int nrb = (rows + 15) >> 4;
+    constexpr int U = WK * JJ;  // units per row (= NU * warps)
+    const int sbytes = 2 * p.ng;
+    const int ps = p.sstride;  // floats per row of the partial and scale tiles: U + 4
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+    float *part = reinterpret_cast<float *>(smem + p.red_off);
+    float *sf = reinterpret_cast<float *>(smem + p.xq_off);
+
+    // ---- 1. weights and scales in flight, the activations toward L2.
+    uint64_t *xbar = &bars[nrb];
+    if (tid == 0) {
+        for (int b = 0; b <= nrb; ++b) mbar_init(&bars[b], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int b = 0; b < nrb; ++b)
+                mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(16, rows - 16 * b) * (p.Kb + sbytes)));
+            prefetch_l2(p.x, (uint32_t)p.x_pref);
+        }
+        __syncwarp();
+        const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
+        for (int r = lane; r < rows; r += 32) {
+            bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb, &bars[r >> 4]);
+            bulk_g2s(smem + p.sc_off + r * sbytes, s16 + (size_t)(row0 + r) * p.ng, (uint32_t)sbytes, &bars[r >> 4]);
+        }
+    }
+
+    // ---- 2. before the wait: the first row block's A fragments, and the
+    // scales as f32 in fold order ([row][chain][j], unit = chain + WK j).
+    // One warp polls the copies; the others sleep in the CTA barrier rather
+    // than take issue slots from the kernel still computing on this SM, and
+    // then check each (completed) phase once for the acquire.
+    const uint32_t woff = 16 * warp * CPG + 4 * t;  // the lane's word in the warp's first chunk
+    bool ok = true;
+    if (warp == 0)
+        for (int b = 0; b < nrb; ++b) ok = mbar_wait_bounded(&bars[b], 0) && ok;
+    __syncthreads();
+    for (int b = 0; b < nrb; ++b) ok = mbar_try_wait(&bars[b], 0) && ok;
+    uint32_t pre[kPre ? NCH : 1][8];
+    if constexpr (kPre) {
+        const uint8_t *w0 = smem + p.w_off + g * p.wstride + woff;
+        const uint8_t *w8 = rows > 8 ? w0 + 8 * p.wstride : w0;
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+            const int o = 16 * (nw * (i / CPG) * CPG + i % CPG);
+            uint32_t a[4], b[4];
+            unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w0 + o), a);
+            unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w8 + o), b);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                pre[i][e] = a[e];
+                pre[i][4 + e] = b[e];
+            }
+        }
+    }
+    {
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(smem + p.sc_off);
+        // U = WK * JJ units per row; thread -> (row, chain, j) with j fastest
+        for (int i = tid; i < rows * U; i += nw * 32) {
+            const int r = i / U, cj = i - r * U;  // U is a compile-time WK * JJ
+            const int c = cj / JJ, j = cj - c * JJ;
+            sf[r * ps + cj] = __half2float(__ushort_as_half(sc[r * p.ng + c + WK * j]));
+        }
+    }
+
+    griddep_wait();  // x may be written, and y read, by the previous kernel
+    if (tid == 0) {
+        // the 16-byte-aligned part of the row (x_pref bytes); a ragged tail is read below
+        mbar_arrive_expect_tx(xbar, (uint32_t)p.x_pref);
+        bulk_g2s(smem + p.x_off, p.x, (uint32_t)p.x_pref, xbar);
+    }
+
+    // ---- 3. the warp's activation chunks as B fragments (lanes 0-3; zero elsewhere).
+    ok = mbar_wait_bounded(xbar, 0) && ok;
+    uint4 xb[NCH];
+#pragma unroll
+    for (int i = 0; i < NCH; ++i) {
+        xb[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (g == 0) {
+            const int u = warp + nw * (i / CPG);
+            const int kk = u * p.unit_k + 32 * (i % CPG) + 8 * t;
+            uint4 v;
+            if (2 * (kk + 8) <= p.x_pref) {
+                v = *reinterpret_cast<const uint4 *>(smem + p.x_off + 2 * kk);
+            } else {
+                const uint16_t *xr = static_cast<const uint16_t *>(p.x) + kk;
+                uint32_t e[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) e[j] = (kk + j < p.K) ? (uint32_t)__ldcg(xr + j) : 0u;
+                v = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16), e[6] | (e[7] << 16));
+            }
+            // (x0 x4)(x1 x5)(x2 x6)(x3 x7): the pair order of unpack_signed_bf16
+            xb[i] = make_uint4(prmt(v.x, v.z, 0x5410), prmt(v.x, v.z, 0x7632), prmt(v.y, v.w, 0x5410),
+                               prmt(v.y, v.w, 0x7632));
+        }
+    }
+
+    // ---- 4. unit partials of every 16-row block.  In a last block of at
+    // most 8 rows the MMA rows g + 8 read row g again; those rows are never
+    // stored, and each MMA row depends only on its own A row.
+    auto store = [&](int rb, int j, const float (&pt)[4]) {
+        if (t == 0) {
+            const int u = warp + nw * j;
+            const int o = (u % WK) * JJ + u / WK;
+            part[(16 * rb + g) * ps + o] = pt[0];
+            if (16 * rb + 8 < rows) part[(16 * rb + g + 8) * ps + o] = pt[2];
+        }
+    };
+    if constexpr (kPre) {
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            float pt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int cc = 0; cc < CPG; ++cc) {
+                const uint32_t(&a)[8] = pre[j * CPG + cc];
+                mma_bf16(pt, a[0], a[4], a[1], a[5], xb[j * CPG + cc].x, xb[j * CPG + cc].y);
+                mma_bf16(pt, a[2], a[6], a[3], a[7], xb[j * CPG + cc].z, xb[j * CPG + cc].w);
+            }
+            store(0, j, pt);
+        }
+    }
+    for (int rb = kPre ? 1 : 0; rb < nrb; ++rb) {
+        const uint8_t *w0 = smem + p.w_off + (16 * rb + g) * p.wstride + woff;
+        const uint8_t *w8 = 16 * rb + 8 < rows ? w0 + 8 * p.wstride : w0;
+#pragma unroll
+        for (int j = 0; j < NU; ++j) {
+            float pt[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+            for (int cc = 0; cc < CPG; ++cc) {
+                const int o = 16 * (nw * j * CPG + cc);  // chunk (warp + nw j) CPG + cc, relative to woff
+                uint32_t pa[4], pb[4];
+                unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w0 + o), pa);
+                unpack_signed_bf16(*reinterpret_cast<const uint32_t *>(w8 + o), pb);
+                mma_bf16(pt, pa[0], pb[0], pa[1], pb[1], xb[j * CPG + cc].x, xb[j * CPG + cc].y);
+                mma_bf16(pt, pa[2], pb[2], pa[3], pb[3], xb[j * CPG + cc].z, xb[j * CPG + cc].w);
+            }
+            store(rb, j, pt);
+        }
+    }
+    if (!__syncthreads_and(ok)) {
+        if (tid == 0 && p.status) atomicOr(p.status, kStatusCopyTimeout);
+        // copies still in flight get one more bounded wait before the CTA's shared memory goes away
+        for (int b = 0; b <= nrb; ++b) (void)mbar_wait_bounded(&bars[b], 0);
+        return;
+    }
+
+    // ---- 5. fold: thread (row, chain c) takes units c, c + WK, ... in order,
+    // acc = fma(s_u, part_u, acc); the WK chains are added in index order.
+    for (int i = tid; i < ((rows * WK + 31) & ~31); i += nw * 32) {
+        const int r = i >> 2, c = i & 3;
+        float acc = 0.0f;
+        if (r < rows) {
+            const float4 *pr = reinterpret_cast<const float4 *>(part + r * ps + c * JJ);
+            const float4 *sr = reinterpret_cast<const float4 *>(sf + r * ps + c * JJ);
+            float4 pv[JJ / 4], sv[JJ / 4];
+#pragma unroll
+            for (int j = 0; j < JJ / 4; ++j) {
+                pv[j] = pr[j];
+                sv[j] = sr[j];
+            }
+#pragma unroll
+            for (int j = 0; j < JJ / 4; ++j) {
+                acc = fmaf(sv[j].x, pv[j].x, acc);
+                acc = fmaf(sv[j].y, pv[j].y, acc);
+                acc = fmaf(sv[j].z, pv[j].z, acc);
+                acc = fmaf(sv[j].w, pv[j].w, acc);
+            }
+        }
+        const float a1 = __shfl_down_sync(0xffffffffu, acc, 1);
+        const float a2 = __shfl_down_sync(0xffffffffu, acc, 2);
+        const float a3 = __shfl_down_sync(0xffffffffu, acc, 3);
+        if (c == 0 && r < rows) p.y[row0 + r] = ((acc + a1) + a2) + a3;
+    }
+}
+
 // ---------------------------------------------------------------- generic fallback
 
 // One warp per output element; any shape, any layout.  Integer kinds are
@@ -1691,6 +1903,28 @@ cudaError_t launch_q4dp(const GemvParams &p, int threads, int smem, cudaStream_t
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int CPG, int NU, int JJ>
+cudaError_t launch_m1_w4a16(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    auto *kern = gemv_m1_w4a16_kernel<CPG, NU, JJ>;
+    std::call_once(once, [kern] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(p.N, p.R), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
 // Warps of the integer-dot kernel: about one per 4 rows of the CTA, 4 to 16
 // (measured: 4 warps for 16 rows and 16 for 88 rows beat the other choice).
 int q4dp_threads(int R) { return 32 * std::max(4, std::min(16, R / 4)); }
@@ -1861,6 +2095,56 @@ bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out,
     return true;
 }
 
+// Plans gemv_m1_w4a16_kernel (W4A16, M = 1, row-major, no K split); false
+// when it does not apply.  p holds the call's geometry with upc = units and
+// the call's WK.  Rows per CTA: a multiple of 8, spread over the fewest
+// waves of 152 CTAs, within two CTAs' worth of shared memory per SM.
+bool plan_m1_w4a16(const LinearArgs &a, GemvParams &p, int &threads, int &smem) {
+    if (a.kind != KIND_W4A16 || a.M != 1 || a.layout != W4_LAYOUT_ROWMAJOR || p.upc != p.units) return false;
+    if (p.WK != 1 && p.WK != 2 && p.WK != 4) return false;
+    if (p.Kb % 16 != 0 || (2 * p.ng) % 16 != 0 || reinterpret_cast<uintptr_t>(a.scale) % 16 != 0) return false;
+    if (p.cpg != 1 && p.cpg != 2 && p.cpg != 4) return false;
+    // every warp takes the same number of units, 4 or 8 chunks: 8 to 16 warps;
+    // the fold reads chains of units/4 in 16-byte vectors
+    const int chunks = p.units * p.cpg;
+    const int nch = chunks <= 64 ? 4 : 8;
+    if (chunks % nch != 0 || chunks / nch > 16 || chunks / nch < 4 || (nch / p.cpg) * (chunks / nch) != p.units)
+        return false;
+    if (p.WK != 4 || p.units % 16 != 0 || p.units > 64) return false;
+    if (reinterpret_cast<uintptr_t>(a.x) % 16 != 0 || a.K < 8) return false;
+    const int cap = kStreamSmemPerCta;
+    p.wstride = pad_to(p.Kb, 16);
+    p.sstride = p.units + 4;  // f32 partials / scales per row: 16-byte rows, the 8 rows a warp stores on distinct banks
+    p.x_al = 1;
+    p.x_pref = (int)((a.K * 2) & ~(int64_t)15);  // bytes of x in the bulk copy
+    auto layout = [&](int R) -> int {
+        int off = 0;
+        p.bar_off = off;
+        off += (int)round_up((int64_t)(ceil_div(R, 16) + 1) * 8, 128);
+        p.w_off = off;
+        off += (int)round_up((int64_t)R * p.wstride, 128);
+        p.sc_off = off;
+        off += (int)round_up((int64_t)R * 2 * p.ng, 128);
+        p.red_off = off;
+        off += (int)round_up((int64_t)R * p.sstride * 4, 128);
+        p.xq_off = off;
+        off += (int)round_up((int64_t)R * p.sstride * 4, 128);
+        p.x_off = off;
+        off += (int)round_up(p.x_pref, 128);
+        return off;
+    };
+    int rmax = 256;
+    while (rmax >= 8 && layout(rmax) > cap) rmax -= 8;
+    if (rmax < 8) return false;
+    const int64_t waves = ceil_div(a.N, (int64_t)152 * rmax);
+    const int R = (int)std::min<int64_t>(rmax, round_up(ceil_div(a.N, 152 * waves), 8));
+    p.R = R;
+    const int off = layout(R);
+    threads = 32 * (chunks / nch);
+    smem = std::max(off, kStreamMinSmem);
+    return true;
+}
+
 }  // namespace
 
 bool gemv_supported(const LinearArgs &a) {
@@ -1987,6 +2271,26 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
                 case 4: return dispatch_stream<KIND_W4A16, 4, false, 2>(q, rb, nrbw, sthreads, ssmem, st, pdl);
                 default: return dispatch_stream<KIND_W4A16, 0, false, 2>(q, rb, nrbw, sthreads, ssmem, st, pdl);
             }
+        }
+    }
+    // W4A16, M = 1, no K split, PDL: every warp of the CTA after the wait (same bits).
+    if (pdl && a.kind == KIND_W4A16 && a.M == 1 && S == 1 && a.N >= 1024) {
+        GemvParams q = p;
+        q.WK = s.WK;
+        q.upc = p.units;
+        int mthreads = 0, msmem = 0;
+        if (plan_m1_w4a16(a, q, mthreads, msmem)) {
+            // (chunks per unit, units per warp, units per fold chain)
+            const int nu = (p.units * p.cpg > 64 ? 8 : 4) / p.cpg, jj = p.units / 4;
+            cudaError_t (*fn)(const GemvParams &, int, int, cudaStream_t, bool) = nullptr;
+            if (p.cpg == 1 && nu == 4 && jj == 16) fn = launch_m1_w4a16<1, 4, 16>;
+            if (p.cpg == 1 && nu == 4 && jj == 8) fn = launch_m1_w4a16<1, 4, 8>;
+            if (p.cpg == 2 && nu == 2 && jj == 8) fn = launch_m1_w4a16<2, 2, 8>;
+            if (p.cpg == 2 && nu == 2 && jj == 4) fn = launch_m1_w4a16<2, 2, 4>;
+            if (p.cpg == 2 && nu == 4 && jj == 16) fn = launch_m1_w4a16<2, 4, 16>;
+            if (p.cpg == 4 && nu == 1 && jj == 4) fn = launch_m1_w4a16<4, 1, 4>;
+            if (p.cpg == 4 && nu == 2 && jj == 8) fn = launch_m1_w4a16<4, 2, 8>;
+            if (fn) return fn(q, mthreads, msmem, st, pdl);
         }
     }
     // Large N, M <= 8, no K split, PDL: the streaming kernel (same arithmetic).
