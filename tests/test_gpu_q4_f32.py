@@ -54,7 +54,7 @@ def check(ops, ora, x, W, flags=0, layout=0):
 @pytest.mark.parametrize("flags", [0, 1])
 @pytest.mark.parametrize("M", [1, 3, 8])
 @pytest.mark.parametrize("N,K", [(2048, 2048), (13312, 2048), (1024, 1024), (2048, 2047), (3072, 4096),
-                                 (512, 2048), (37, 200), (1024, 1000)])
+                                 (512, 2048), (37, 200), (1024, 1000), (1100, 1056), (1536, 2040), (4099, 2045)])
 def test_linear_q4_f32_bitexact(ops, ora, flags, M, N, K):
     x = synth.activations_f32(151 + M + K, M, K)
     W = synth.weights_f32(152 + N + K, N, K)

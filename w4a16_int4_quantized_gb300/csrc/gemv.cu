@@ -1690,6 +1690,216 @@ __global__ void __launch_bounds__(512, 2) gemv_m1_w4a16_kernel(const __grid_cons
     }
 }
 
+// ---------------------------------------------------------------- W4A8, one activation row, all warps
+//
+// linear_q4 at M = 1 under PDL ("Q4 weights x Q8 activations": acc = sum_k
+// xq * u - 8 * sum_k xq, exact in i32; y = (f32(acc) * sx) * sw), laid out
+// like gemv_m1_w4a16_kernel: each CTA's weight rows arrive by bulk copies
+// before griddepcontrol.wait and each warp's first row is loaded into
+// registers there; the activation row (f32 for the fused quantize + linear
+// call, else Q8 codes) is asked into L2 before the wait and brought into
+// shared memory by one bulk copy after it.  XQ: every CTA quantises the row
+// with quantize_row_q8's arithmetic (one 4-column vector per thread: amax
+// through one CTA barrier, sx = fl(amax / 127), codes rint(fl(v / sx)) by a
+// reciprocal with an exact-division fallback near ties) and CTA 0 writes the
+// codes and the scale out.  Then warp w takes rows w, w + 16, ...: each lane
+// dp4a's the low and high nibbles of its 16-byte chunks against the even and
+// odd codes.  The result is an exact integer, so any order gives the same bits.
+template <bool XQ, int CH>
+__global__ void __launch_bounds__(512, 2) gemv_m1_q4_kernel(const __grid_constant__ GemvParams p) {
+    griddep_launch_dependents();
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int nthr = nw * 32;
+    const int row0 = blockIdx.x * p.R;
+    const int rows = min(p.R, p.N - row0);
+    const int nrb = (rows + 15) >> 4;
+    const int chunks = p.Kb >> 4;  // 16-byte weight chunks (32 columns) per row
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.bar_off);
+    uint64_t *xbar = &bars[nrb];
+    const uint8_t *xq_s = smem + p.xq_off;  // codes as (even, odd) words per 8 columns
+
+    // ---- 1. weight rows in flight, the activations toward L2.
+    if (tid == 0) {
+        for (int b = 0; b <= nrb; ++b) mbar_init(&bars[b], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int b = 0; b < nrb; ++b) mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(16, rows - 16 * b) * p.Kb));
+            prefetch_l2(XQ ? static_cast<const void *>(p.xf) : p.x, (uint32_t)p.x_pref);
+        }
+        __syncwarp();
+        for (int r = lane; r < rows; r += 32)
+            bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb, &bars[r >> 4]);
+    }
+    // one warp polls the copies, the others sleep in the CTA barrier
+    bool ok = true;
+    if (warp == 0)
+        for (int b = 0; b < nrb; ++b) ok = mbar_wait_bounded(&bars[b], 0) && ok;
+    __syncthreads();
+    for (int b = 0; b < nrb; ++b) ok = mbar_try_wait(&bars[b], 0) && ok;
+    uint4 w1[CH];  // the warp's first row
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int c = lane + 32 * i;
+        w1[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < chunks && warp < rows) w1[i] = lds_u128(smem_u32(smem + p.w_off + warp * p.wstride + 16 * c));
+    }
+
+    griddep_wait();  // x may be written, and y read, by the previous kernel
+    if (tid == 0) {
+        mbar_arrive_expect_tx(xbar, (uint32_t)p.x_pref);
+        bulk_g2s(smem + p.x_off, XQ ? static_cast<const void *>(p.xf) : p.x, (uint32_t)p.x_pref, xbar);
+    }
+    ok = mbar_wait_bounded(xbar, 0) && ok;
+    const int K = p.K;
+    const int ncols = 32 * chunks;  // codes staged, zero beyond K
+
+    // ---- 2. the Q8 codes as (even, odd) words of each 8-column group.
+    float sx;
+    if constexpr (XQ) {
+        float *red = reinterpret_cast<float *>(smem + p.red_off);
+        const float *xs = reinterpret_cast<const float *>(smem + p.x_off);
+        float4 v[2];
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int k = 4 * (tid + i * nthr);
+            v[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (4 * (k + 4) <= p.x_pref) {
+                v[i] = *reinterpret_cast<const float4 *>(xs + k);
+            } else if (k < K) {
+                v[i].x = p.xf[k];
+                if (k + 1 < K) v[i].y = p.xf[k + 1];
+                if (k + 2 < K) v[i].z = p.xf[k + 2];
+                if (k + 3 < K) v[i].w = p.xf[k + 3];
+            }
+            am = fmaxf(am, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) red[warp] = am;
+        __syncthreads();
+        am = red[0];
+        for (int w2 = 1; w2 < nw; ++w2) am = fmaxf(am, red[w2]);
+        sx = __fdiv_rn(am, 127.0f);
+        // Codes clamp(rint(fl(v / sx)), -127, 127) by t = fl(v * r), r = fl(1 / sx):
+        // t lies within 2^-15 of fl(v / sx) when |v / sx| < 256 (two correctly
+        // rounded operations), so rint(t) is rint(fl(v / sx)) unless t is within
+        // 2^-13 of a half-integer; those values (and all of them when 1 / sx
+        // overflows) take the IEEE quotient.
+        const float r = sx != 0.0f ? __frcp_rn(sx) : 0.0f;
+        const bool fast = isfinite(r);
+        const bool out = blockIdx.x == 0 && p.xq_out != nullptr;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int k = 4 * (tid + i * nthr);
+            const float e[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t c4 = 0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float tq = __fmul_rn(e[q], r);
+                const float rt = rintf(tq);
+                int c = 0;
+                if (sx != 0.0f) {
+                    if (fast && fabsf(tq) < 256.0f && 0.5f - fabsf(tq - rt) > 0x1p-13f) c = __float2int_rn(rt);
+                    else c = __float2int_rn(__fdiv_rn(e[q], sx));
+                    c = min(max(c, -127), 127);
+                }
+                c4 |= (uint32_t)(uint8_t)(int8_t)c << (8 * q);
+            }
+            // the partner lane holds the other half of the 8-column group
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, c4, 1);
+            if (k < ncols && (tid & 1) == 0)
+                *reinterpret_cast<uint2 *>(const_cast<uint8_t *>(xq_s) + k) = even_odd(c4, other);
+            if (out) {
+                if (k + 3 < K) {
+                    *reinterpret_cast<uint32_t *>(p.xq_out + k) = c4;  // k % 4 == 0 and xq_out 4-byte aligned
+                } else {
+                    for (int q = 0; q < 4 && k + q < K; ++q) p.xq_out[k + q] = (int8_t)(c4 >> (8 * q));
+                }
+            }
+        }
+        if (out && tid == 0 && p.sx_out) p.sx_out[0] = sx;
+        __syncthreads();
+    } else {
+        sx = p.sx[0];
+    }
+
+    // ---- 3. the lane's activation chunks (c = lane + 32 i) and their code sum.
+    uint4 xe[CH], xo[CH];
+    int xsum = 0;
+#pragma unroll
+    for (int i = 0; i < CH; ++i) {
+        const int c = lane + 32 * i;
+        xe[i] = make_uint4(0u, 0u, 0u, 0u);
+        xo[i] = xe[i];
+        if (c < chunks) {
+            if constexpr (XQ) {
+                const uint4 a = lds_u128(smem_u32(xq_s + 32 * c));
+                const uint4 b = lds_u128(smem_u32(xq_s + 32 * c + 16));
+                xe[i] = make_uint4(a.x, a.z, b.x, b.z);
+                xo[i] = make_uint4(a.y, a.w, b.y, b.w);
+            } else {
+                // raw Q8 codes; zero beyond K
+                uint32_t wv[8];
+                const int k0 = 32 * c;
+                if (k0 + 32 <= p.x_pref) {
+                    const uint4 a = lds_u128(smem_u32(smem + p.x_off + k0));
+                    const uint4 b = lds_u128(smem_u32(smem + p.x_off + k0 + 16));
+                    wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w;
+                    wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
+                } else {
+                    const int8_t *xr = static_cast<const int8_t *>(p.x);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t wd = 0;
+                        for (int q = 0; q < 4; ++q) {
+                            const int k = k0 + 4 * j + q;
+                            const uint32_t b8 = k < p.x_pref ? smem[p.x_off + k] : (k < K ? (uint8_t)xr[k] : 0u);
+                            wd |= b8 << (8 * q);
+                        }
+                        wv[j] = wd;
+                    }
+                }
+                const uint2 g0 = even_odd(wv[0], wv[1]), g1 = even_odd(wv[2], wv[3]);
+                const uint2 g2 = even_odd(wv[4], wv[5]), g3 = even_odd(wv[6], wv[7]);
+                xe[i] = make_uint4(g0.x, g1.x, g2.x, g3.x);
+                xo[i] = make_uint4(g0.y, g1.y, g2.y, g3.y);
+            }
+        }
+        xsum = sum_chunk_dp(xe[i], xo[i], xsum);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) xsum += __shfl_xor_sync(0xffffffffu, xsum, o);
+
+    // ---- 4. rows: exact integer dot products, one warp per row.
+    const float *sw = static_cast<const float *>(p.scale);
+    for (int r = warp; r < rows; r += nw) {
+        int acc = 0;
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+            const int c = lane + 32 * i;
+            if (c < chunks) {
+                const uint4 wv = r == warp ? w1[i] : lds_u128(smem_u32(smem + p.w_off + r * p.wstride + 16 * c));
+                acc = dot_chunk_dp(wv, xe[i], xo[i], acc);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0 && ok) {
+            const int n = row0 + r;
+            p.y[n] = __fmul_rn(__fmul_rn(__int2float_rn(acc - 8 * xsum), sx), sw[n]);
+        }
+    }
+    if (!ok) {
+        if (lane == 0 && p.status) atomicOr(p.status, kStatusCopyTimeout);
+        for (int b = 0; b <= nrb; ++b) (void)mbar_wait_bounded(&bars[b], 0);
+    }
+}
+
 // ---------------------------------------------------------------- generic fallback
 
 // One warp per output element; any shape, any layout.  Integer kinds are
@@ -1925,6 +2135,36 @@ cudaError_t launch_m1_w4a16(const GemvParams &p, int threads, int smem, cudaStre
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <bool XQ, int CH>
+cudaError_t launch_m1_q4(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    auto *kern = gemv_m1_q4_kernel<XQ, CH>;
+    std::call_once(once, [kern] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(p.N, p.R), 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1u : 0u;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <bool XQ>
+cudaError_t dispatch_m1_q4(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+    const int chunks = p.Kb >> 4;
+    if (chunks <= 32) return launch_m1_q4<XQ, 1>(p, threads, smem, st, pdl);
+    if (chunks <= 64) return launch_m1_q4<XQ, 2>(p, threads, smem, st, pdl);
+    return launch_m1_q4<XQ, 4>(p, threads, smem, st, pdl);
+}
+
 // Warps of the integer-dot kernel: about one per 4 rows of the CTA, 4 to 16
 // (measured: 4 warps for 16 rows and 16 for 88 rows beat the other choice).
 int q4dp_threads(int R) { return 32 * std::max(4, std::min(16, R / 4)); }
@@ -2145,6 +2385,37 @@ bool plan_m1_w4a16(const LinearArgs &a, GemvParams &p, int &threads, int &smem) 
     return true;
 }
 
+// Plans gemv_m1_q4_kernel (W4A8, M = 1, row-major, K <= 4096); false when it
+// does not apply.  xq: the fused call (f32 activations quantised in the CTAs).
+bool plan_m1_q4(const LinearArgs &a, GemvParams &p, bool xq, int &threads, int &smem) {
+    if (a.kind != KIND_W4A8 || a.M != 1 || a.layout != W4_LAYOUT_ROWMAJOR || a.N < 1024) return false;
+    if (p.Kb % 16 != 0 || (p.Kb >> 4) > 128) return false;
+    const void *x = xq ? static_cast<const void *>(a.xf) : a.x;
+    if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return false;
+    if (xq && a.xq_out && reinterpret_cast<uintptr_t>(a.xq_out) % 4 != 0) return false;
+    const int cap = kStreamSmemPerCta;
+    p.wstride = pad_to(p.Kb, 16);
+    p.x_pref = (int)((a.K * (xq ? 4 : 1)) & ~(int64_t)15);
+    const int ncols = 2 * p.Kb;
+    const int R = (int)ceil_div(a.N, 152);
+    int off = 0;
+    p.bar_off = off;
+    off += (int)round_up((ceil_div(R, 16) + 1) * 8, 128);
+    p.w_off = off;
+    off += (int)round_up((int64_t)R * p.wstride, 128);
+    p.x_off = off;
+    off += (int)round_up(std::max(p.x_pref, 16), 128);
+    p.xq_off = off;
+    if (xq) off += (int)round_up(ncols, 128);
+    p.red_off = off;
+    off += 128;
+    if (off > cap) return false;
+    p.R = R;
+    threads = 512;
+    smem = std::max(off, kStreamMinSmem);
+    return true;
+}
+
 }  // namespace
 
 bool gemv_supported(const LinearArgs &a) {
@@ -2224,6 +2495,15 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     if (a.xf) {
         GemvParams q = p;
         q.WK = s.WK;
+        int mthreads = 0, msmem = 0;
+        if (plan_m1_q4(a, q, true, mthreads, msmem)) {
+            q.xf = a.xf;
+            q.xq_out = a.xq_out;
+            q.sx_out = a.sx_out;
+            return dispatch_m1_q4<true>(q, mthreads, msmem, st, (a.flags & W4_FLAG_PDL) != 0);
+        }
+        q = p;
+        q.WK = s.WK;
         int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
         // M = 1 only: more rows take the per-element quantiser path, slower
         // inside every CTA than the separate quantizer kernel
@@ -2250,7 +2530,12 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     s.S = S;
     const int threads = 32 * p.WR * p.WK;
     const bool pdl = (a.flags & W4_FLAG_PDL) != 0;
-    // W4A8, M = 1, large N, no K split, PDL: the integer-dot streaming kernel.
+    // W4A8, M = 1, PDL: the all-warp integer-dot kernel, else the streaming one.
+    if (pdl && a.kind == KIND_W4A8 && a.M == 1) {
+        GemvParams q = p;
+        int mthreads = 0, msmem = 0;
+        if (plan_m1_q4(a, q, false, mthreads, msmem)) return dispatch_m1_q4<false>(q, mthreads, msmem, st, pdl);
+    }
     if (pdl && a.kind == KIND_W4A8 && a.M == 1 && a.layout == W4_LAYOUT_ROWMAJOR && S == 1 && (p.Kb >> 4) <= 128) {
         GemvParams q = p;
         int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
