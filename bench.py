@@ -24,6 +24,7 @@ import argparse
 import datetime as _dt
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -93,6 +94,27 @@ WORKLOADS = {
     "w4a8g_prefill_m2048_n13312": _wl("w4a8g", 2048, 13312, 2048, 128, 0,
                                       "grouped asymmetric W4A8 prefill M=2048, K=2048, N=13312, G=128"),
 }
+
+# The decode-batch configuration: M in {1, 4, 16}, K = 2048, N in {13312 (gate_up), 3072}, W4A16 (G = 128) and
+# W4A8, row-major and interleaved [N/64][K][32] weights.
+for _kind in ("w4a16", "w4a8"):
+    for _M in (1, 4, 16):
+        for _N in (13312, 3072):
+            for _lay in (0, 1):
+                _name = f"{_kind}_decode_m{_M}_n{_N}" + ("_il" if _lay else "")
+                if _name not in WORKLOADS:
+                    WORKLOADS[_name] = _wl(
+                        _kind, _M, _N, 2048, 128 if _kind == "w4a16" else 0, _lay,
+                        f"{'W4A16' if _kind == 'w4a16' else 'W4A8'} decode M={_M}, K=2048, N={_N}"
+                        + (", G=128" if _kind == "w4a16" else "") + (", interleaved [N/64][K][32] layout" if _lay else ""))
+
+# Extra lines of the default run: every configuration of the benchmark set
+# beside the headline (odd K, the decode batch grid, the prefill GEMMs).
+EXTRA_DECODE = (["w4a16_gemv_m1_k2047", "w4a8_gemv_m1"]
+                + [f"{k}_decode_m{m}_n{n}{l}" for k in ("w4a16", "w4a8") for m in (1, 4, 16) for n in (13312, 3072)
+                   for l in ("", "_il")])
+EXTRA_PREFILL = ([f"{k}_prefill_m2048_n{n}" for k in ("w4a8", "w4a16") for n in (2048, 3072, 13312)]
+                 + ["w4a8_prefill_m2048_n13312_il", "w4a16_prefill_m2048_n13312_il"])
 
 
 # DRAM bytes (read + write) per launch of the roofline's kernel from one ncu
@@ -316,6 +338,8 @@ def time_oracle(w, seconds: float, openmp: bool = True):
             break
     value, unit = metric_of(w, el * 1e3 / n)
     sample = f"{n} full calls of {what} on {w['desc']} ({el:.1f} s)"
+    if w.get("layout") == 1:
+        sample += "; the oracle reads the row-major form of the same codes"
     if w["regime"] == "prefill":
         sample = f"{n} calls of {what} on 16 of the {w['desc']} activation rows ({el:.1f} s), as ops/s"
     return {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}, n, el
@@ -606,78 +630,69 @@ def time_e2e(w, steps: int, chunk: int = 64):
                    f"{chunk} steps replayed"}
 
 
-def prefill_lines(peaks):
-    """W4A8 / W4A16 prefill (M = 2048, K = 2048, N in {2048, 3072, 13312}): ops/s of the tensor path."""
-    import torch
-    from w4a16_int4_quantized_gb300 import ops, synth
-    out = []
-    M, K, G = 2048, 2048, 128
-    bf16_peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
-    int8_peak = ops.probe_mma_peak(0)
-    for N in (2048, 3072, 13312):
-        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
-        x, W = synth.w4a8_inputs(1005, M, N, K)
-        xq, sx, _ = ops.quantize_row_q8(dev(x))
-        wq, sw = ops.quantize_matrix_q4(dev(W))
-        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
-        ws = torch.empty(ops.workspace_bytes(ops.OP_LINEAR_Q4, M, N, K), dtype=torch.uint8, device="cuda")
-        xb, wb, sb = synth.w4a16_inputs(1006, M, N, K, G)
-        xbd, wbd, sbd = dev(xb), dev(wb), dev(sb)
-        runs = {
-            "w4a8": lambda: ops.linear_q4(xq, sx, wq, sw, K=K, out=y, workspace=ws),
-            "w4a16": lambda: ops.linear_w4a16_group(xbd, wbd, sbd, G, K=K, out=y),
-        }
-        if N == 13312:
-            # prefill straight from the interleaved layout, same codes
-            wq_il, wb_il = ops.pack_interleaved_n64(wq, K), ops.pack_interleaved_n64(wbd, K)
-            runs["w4a8_il"] = lambda: ops.linear_q4(xq, sx, wq_il, sw, K=K, N=N, layout=ops.LAYOUT_N64, out=y,
-                                                    workspace=ws)
-            runs["w4a16_il"] = lambda: ops.linear_w4a16_group(xbd, wb_il, sbd, G, K=K, N=N, layout=ops.LAYOUT_N64,
-                                                              out=y)
-        for name, fn in runs.items():
-            for _ in range(3):
-                fn()
-            torch.cuda.synchronize()
-            reps = 20
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(reps):
-                fn()
-            e1.record()
-            e1.synchronize()
-            ms = e0.elapsed_time(e1) / reps
-            tops = 2.0 * M * N * K / (ms / 1e3) / 1e12
-            kind, _, lay = name.partition("_")
-            out.append({"workload": f"{kind}_prefill_m{M}_n{N}_k{K}" + (f"_{lay}" if lay else ""),
-                        "metric": "TOPS" if kind == "w4a8" else "TFLOP/s",
-                        "value": round(tops, 1), "ms_per_call": round(ms, 4),
-                        "roofline": {"bound": "tensor", "achieved": round(tops, 1), "peak": bf16_peak, "unit": "TFLOP/s",
-                                     "frac": round(tops / bf16_peak, 4),
-                                     "note": "f16/bf16 tcgen05 path; peak = measured bf16 dense sustained (f16 same rate)"}})
-            if kind == "w4a8":
-                out[-1]["roofline"]["int8_mma_sync_peak_tops"] = round(int8_peak, 1)
-                out[-1]["roofline"]["frac_of_int8_peak"] = round(tops / int8_peak, 3)
-        del xq, wq, y, ws, xbd, wbd, sbd
-        torch.cuda.empty_cache()
-    return out
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
 
 
-def extra_lines(l2: int, peak_gbs: float):
+def measure_line(name: str, l2: int, peaks, sampler, cpu_seconds: float | None):
+    """One workload of the benchmark set: the step (the whole hot path) and the
+    roofline's kernel alone, both from CUDA-graph replays over rotating inputs
+    larger than L2, with the clocks seen and the oracle timed on a bounded sample."""
     import torch
-    out = []
-    for name in ("w4a8_gemv_m1", "w4a16_decode_m16_n13312", "w4a16_decode_m1_n13312_il", "w4a8_decode_m16_n13312"):
-        w = WORKLOADS[name]
-        wl = Workload(w, copies_for(w, l2))
-        steps = 2048
-        ms, _, _ = time_steps(wl, steps, 3)
-        gbs = steps * weight_bytes(w) / (ms / 1e3) / 1e9
-        ach = step_bytes(w) / (ms / 1e3 / steps) / 1e9
-        out.append({"workload": name, "desc": w["desc"], "metric": "int4 linear weight GB/s",
-                    "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(ms * 1e3 / steps, 3),
-                    "roofline": {"bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs,
-                                 "frac": round(ach / peak_gbs, 4)}})
-        del wl
-        torch.cuda.empty_cache()
+    from w4a16_int4_quantized_gb300 import ops
+    w = WORKLOADS[name]
+    wl = Workload(w, copies_for(w, l2))
+    steps = 2048 if w["regime"] == "decode" else 32
+    ms, t0, t1 = time_steps(wl, steps, 3)
+    kms, _, _ = time_steps(wl, steps, 3, kernel_only=True)
+    value, unit = metric_of(w, ms / steps)
+    per_launch = kms / 1e3 / steps
+    if w["regime"] == "decode":
+        peak = float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))
+        ach = step_bytes(w) / per_launch / 1e9
+        roof = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                "traffic": TRAFFIC.get(name), "bytes_per_launch": step_bytes(w),
+                "us_per_launch": round(per_launch * 1e6, 3), "peak_source": "measured hbm_gbs (copy)"}
+    else:
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        ach = step_ops(w) / per_launch / 1e12
+        roof = {"bound": "tensor", "achieved": round(ach, 1), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(ach / peak, 4), "traffic": TRAFFIC.get(name), "flops_per_launch": step_ops(w),
+                "us_per_launch": round(per_launch * 1e6, 3),
+                "peak_source": "measured bf16_tflops (burst: the call is timed on its own; kind::f16 runs at the "
+                               "bf16 rate)"}
+    line = {"workload": name, "desc": w["desc"], "metric": metric_name(w), "value": round(value, 2), "unit": unit,
+            "us_per_step": round(ms * 1e3 / steps, 3), "steps": steps, "launches_per_step": wl.launches_per_step,
+            "roofline": roof, "clocks": sampler.summary(t0, t1)}
+    if w["kind"] == "w4a8" and w["regime"] == "prefill":
+        line["step"] = "quantize_row_q8 + linear_q4 (linear_q4_f32); roofline: linear_q4 alone (int8 -> f16 prepass + GEMM)"
+        kv, _ = metric_of(w, kms / steps)
+        line["linear_only"] = {"value": round(kv, 2), "unit": unit, "us_per_call": round(per_launch * 1e6, 3)}
+    del wl
+    torch.cuda.empty_cache()
+    if cpu_seconds:
+        cb, _, _ = time_oracle(w, cpu_seconds)
+        cb["cpu_model"] = cpu_model()
+        line["cpu_baseline"] = cb
+    return line
+
+
+def extra_lines(l2: int, peaks, sampler, cpu_seconds: float | None):
+    out = [measure_line(n, l2, peaks, sampler, cpu_seconds) for n in EXTRA_DECODE + EXTRA_PREFILL]
+    from w4a16_int4_quantized_gb300 import ops
+    int8 = ops.probe_mma_peak(0)
+    for ln in out:
+        if ln["workload"].startswith("w4a8_prefill"):
+            ln["roofline"]["int8_mma_sync_peak_tops"] = round(int8, 1)
+            ln["roofline"]["frac_of_int8_peak"] = round(ln["roofline"]["achieved"] / int8, 3)
     return out
 
 
@@ -1027,6 +1042,7 @@ def run_microdecoder(args, world, rank, local):
     cpu = None
     if not args.no_cpu:
         cpu, _, _ = time_oracle_microdecoder(args.cpu_seconds)
+        cpu["cpu_model"] = cpu_model()
     line = {"metric": "microdecoder effective int4 weight GB/s (frame)", "value": round(value, 1), "unit": "GB/s",
             "n_gpus": world, "steps": frames, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "s8", "data": "synthetic",
@@ -1082,7 +1098,16 @@ def run_ours(args, world, rank, local):
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
-    ms, t0, t1 = time_steps(wl, args.steps, args.warmup)
+    # the timed region (exactly `steps` steps) is run `repeats` times; the
+    # median is reported, the individual times beside it
+    runs = []
+    for r in range(max(1, args.repeats)):
+        ms_r, t0_r, t1_r = time_steps(wl, args.steps, args.warmup)
+        runs.append(ms_r)
+        if r == 0:
+            t0 = t0_r
+        t1 = t1_r
+    ms = statistics.median(runs)
     torch.cuda.synchronize()
     time.sleep(0.2)
     sampler.stop()
@@ -1124,16 +1149,22 @@ def run_ours(args, world, rank, local):
     cpu = None
     if not args.no_cpu:
         cpu, _, _ = time_oracle(w, args.cpu_seconds)
+        cpu["cpu_model"] = cpu_model()
     extra = []
     if not args.no_extra and args.workload == "w4a16_gemv_m1":
-        extra = extra_lines(l2, float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS))) + prefill_lines(peaks)
+        sampler = ClockSampler(gpu_id)
+        sampler.start()
+        time.sleep(0.3)
+        extra = extra_lines(l2, peaks, sampler, None if args.no_cpu else min(args.cpu_seconds, 1.0))
+        sampler.stop()
         md, _, _ = microdecoder_line(l2, float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS)), 200, 3)
         extra.append({"workload": MICRODECODER, "desc": MICRODECODER_DESC, "metric": "effective int4 weight GB/s",
                       **{k: {kk: vv for kk, vv in v.items() if kk not in ("t0", "t1")} for k, v in md.items()}})
     line = {
         "metric": metric_name(w),
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": ms_max / args.steps, "repeats": len(runs),
+        "ms_per_step_each": [round(r / args.steps, 7) for r in runs], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"w4a16": "bf16", "w8a16": "f32"}.get(w["kind"], "s8"), "data": "synthetic",
         "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"], "N": w["N"], "K": w["K"],
                    "G": w["G"], "parallelism": "replicas" if world > 1 else "single",
@@ -1143,7 +1174,8 @@ def run_ours(args, world, rank, local):
                             "w4a8g": "quantize_row_q8 + linear_q4_group",
                             "w8a16": "linear_w8a16"}.get(
                        w["kind"], "linear_w4a16_group"),
-                   "timing": "CUDA events around CUDA-graph replays of exactly `steps` steps"},
+                   "timing": "CUDA events around CUDA-graph replays of exactly `steps` steps; the timed region "
+                             "is repeated `repeats` times and the median reported"},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -1165,6 +1197,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--repeats", type=int, default=7)
     args = ap.parse_args()
     if args.impl == "reference":
         world = int(os.environ.get("WORLD_SIZE", "1"))
