@@ -300,6 +300,21 @@ typedef struct w4_chain_linear {
 w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
                       int32_t pass_output, void *workspace, size_t ws_bytes, void *stream);
 
+/* Test entry point of the failure path of w4_chain_q4 (the pages have no
+ * counterpart).  The same chain and arguments, with every wait of the kernel
+ * limited to wait_limit_ns (1 .. 1e9) instead of about one second, and, when
+ * hold_stage >= 0, global stage hold_stage (stage index + pass * stages per
+ * pass; the stages are the linears grouped by depth) computing its outputs
+ * without ever publishing them, so the waits of the stages that read them run
+ * out.  The kernel then sets status bit 4 (w4_device_status) and returns;
+ * outputs of the stages after the held one are left unspecified.  With
+ * hold_stage = -1 the call is w4_chain_q4 with a shorter limit.  For tests of
+ * the timeout path; not part of a production call sequence.
+ * EINVAL: wait_limit_ns out of range or hold_stage < -1; otherwise as w4_chain_q4. */
+w4_status w4_chain_q4_test_timeout(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin,
+                                   int32_t passes, int32_t pass_output, void *workspace, size_t ws_bytes,
+                                   uint64_t wait_limit_ns, int32_t hold_stage, void *stream);
+
 /* Bytes of workspace w4_chain_q4 needs for this chain: 256 + 8 * (2 * K0 +
  * the N of every linear some other linear reads).  Host only; 0 when lin is
  * NULL or n_lin is out of range. */

@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "w4.h"
+#include "common.cuh"
 #include "internal.h"
 
 namespace {
@@ -276,8 +277,9 @@ w4_status w4_pack_interleaved_n64(const uint8_t *w_rowmajor, uint8_t *w_il, int6
     return cuda_status(w4::launch_pack_n64(w_rowmajor, w_il, N, K, as_stream(stream)));
 }
 
-w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
-                      int32_t pass_output, void *workspace, size_t ws_bytes, void *stream) {
+static w4_status chain_q4_impl(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
+                               int32_t pass_output, void *workspace, size_t ws_bytes, void *stream, uint64_t wait_ns,
+                               int32_t hold_stage) {
     if (n_lin < 1 || n_lin > W4_CHAIN_MAX_LINEARS || passes < 0 || K0 <= 0 || !lin) return W4_EINVAL;
     if (pass_output < 0 || pass_output >= n_lin) return W4_EINVAL;
     for (int32_t i = 0; i < n_lin; ++i) {
@@ -305,9 +307,22 @@ w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, i
     cudaError_t e = status_ptr(&status);
     if (e != cudaSuccess) return cuda_status(e);
     const int rc = w4::chain_plan_launch(x0, K0, lin, n_lin, passes, pass_output, workspace, status,
-                                         as_stream(stream), &e);
+                                         as_stream(stream), &e, wait_ns, hold_stage);
     if (rc == W4_ECUDA) return cuda_status(e);
     return (w4_status)rc;
+}
+
+w4_status w4_chain_q4(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
+                      int32_t pass_output, void *workspace, size_t ws_bytes, void *stream) {
+    return chain_q4_impl(x0, K0, lin, n_lin, passes, pass_output, workspace, ws_bytes, stream, w4::kWaitLimitNs, -1);
+}
+
+w4_status w4_chain_q4_test_timeout(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin,
+                                   int32_t passes, int32_t pass_output, void *workspace, size_t ws_bytes,
+                                   uint64_t wait_limit_ns, int32_t hold_stage, void *stream) {
+    if (wait_limit_ns == 0 || wait_limit_ns > w4::kWaitLimitNs || hold_stage < -1) return W4_EINVAL;
+    return chain_q4_impl(x0, K0, lin, n_lin, passes, pass_output, workspace, ws_bytes, stream, wait_limit_ns,
+                         hold_stage);
 }
 
 w4_status w4_pack_block32(const uint8_t *w_rowmajor, const uint16_t *scales_f16, uint8_t *blocks, int64_t N,

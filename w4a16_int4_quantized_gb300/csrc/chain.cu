@@ -73,6 +73,8 @@ struct ChainParams {
     int32_t pass_output;  // sorted index
     int32_t s_out;        // stage of the pass output
     int32_t K0;
+    int32_t hold_stage;   // test of the failure path: this global stage never publishes its outputs (-1: none)
+    uint64_t wait_ns;     // limit of every wait (kWaitLimitNs; shorter in the failure-path test)
 };
 static_assert(sizeof(ChainParams) <= 4096, "kernel parameters");
 
@@ -328,7 +330,7 @@ W4_DEV void compute_stage(const ChainLin *lin, const ChainStage &S, int pass_out
 
 // Input pair j (elements 2j, 2j+1) from a tagged buffer: spins until both
 // carry `want`; false if that takes longer than the wait limit.
-W4_DEV bool wait_pair(const uint64_t *src, uint32_t want, ulonglong2 &a) {
+W4_DEV bool wait_pair(const uint64_t *src, uint32_t want, ulonglong2 &a, uint64_t limit_ns) {
     const auto ok = [&]() { return (uint32_t)(a.x >> 32) == want && (uint32_t)(a.y >> 32) == want; };
     if (ok()) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -336,7 +338,7 @@ W4_DEV bool wait_pair(const uint64_t *src, uint32_t want, ulonglong2 &a) {
         __nanosleep(64);  // fewer requests on the lines every CTA polls: measured best of 0-512 ns
         a = ld_relaxed_gpu_v2(src);
         if (ok()) return true;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -381,7 +383,7 @@ W4_DEV bool run_stage(const ChainParams &p, const ChainLin *lin, const ChainStag
 #pragma unroll
         for (int u = 0; u < KV; ++u) {
             const int j = threadIdx.x + u * kThreads;
-            if (j < n2) good = good && wait_pair(tin + 2 * j, want, a[u]);
+            if (j < n2) good = good && wait_pair(tin + 2 * j, want, a[u], p.wait_ns);
             v[u] = make_float2(__uint_as_float((uint32_t)a[u].x), __uint_as_float((uint32_t)a[u].y));
         }
         if (!good) {
@@ -424,7 +426,8 @@ W4_DEV bool run_stage(const ChainParams &p, const ChainLin *lin, const ChainStag
     __syncthreads();
 
     RowSink k;
-    k.tag = (uint32_t)(gs + 1);
+    // tag 0 is what the cleared workspace holds: a held stage's outputs never appear
+    k.tag = gs == p.hold_stage ? 0u : (uint32_t)(gs + 1);
     k.pout = pass + 1 < p.passes ? p.pbuf + (size_t)(pass & 1) * p.K0 : nullptr;
     compute_stage<ROUNDS>(lin, S, p.pass_output, gw, nw, lane, pf, xs, sx, k);
     return true;
@@ -458,7 +461,7 @@ W4_DEV bool grid_barrier(const ChainParams &p, uint32_t gen, int *abort_flag) {
             while (true) {
                 v = ld_acquire_gpu(p.bar);
                 if ((v & ~kAbortBit) >= target || (v & kAbortBit)) break;
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                if (globaltimer_ns() - t0 > p.wait_ns) {
                     atomicOr(p.bar, kAbortBit);
                     atomicOr(p.status, kStatusBarrierTimeout);
                     v = kAbortBit;
@@ -545,7 +548,8 @@ size_t chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32_t 
 }
 
 int chain_plan_launch(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
-                      int32_t pass_output, void *workspace, uint32_t *status, cudaStream_t st, cudaError_t *err) {
+                      int32_t pass_output, void *workspace, uint32_t *status, cudaStream_t st, cudaError_t *err,
+                      uint64_t wait_ns, int32_t hold_stage) {
     *err = cudaSuccess;
     if (!chain_stages_ok(lin, n_lin, passes, pass_output)) return W4_ESHAPE;
     std::vector<int> depth(n_lin);
@@ -603,6 +607,8 @@ int chain_plan_launch(const float *x0, int32_t K0, const w4_chain_linear *lin, i
     p.pass_output = sorted_of[pass_output];
     p.s_out = depth[pass_output];
     p.K0 = K0;
+    p.hold_stage = hold_stage;
+    p.wait_ns = wait_ns;
     const size_t ws_used = (size_t)(reinterpret_cast<uint8_t *>(next_tag) - ws);
 
     int dev = 0, sms = 0, occ = 0;

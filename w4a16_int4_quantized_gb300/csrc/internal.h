@@ -76,7 +76,10 @@ size_t chain_workspace_bytes(const w4_chain_linear *lin, int32_t n_lin, int32_t 
 bool chain_stages_ok(const w4_chain_linear *lin, int32_t n_lin, int32_t passes, int32_t pass_output);
 // Plans (stages by depth) and launches a validated chain; returns a w4_status
 // (W4_ESHAPE when the chain has no stage structure), *err the CUDA error.
+// wait_ns bounds every wait of the kernel; hold_stage >= 0 (the failure-path
+// test only) keeps that global stage's outputs from ever being published.
 int chain_plan_launch(const float *x0, int32_t K0, const w4_chain_linear *lin, int32_t n_lin, int32_t passes,
-                      int32_t pass_output, void *workspace, uint32_t *status, cudaStream_t st, cudaError_t *err);
+                      int32_t pass_output, void *workspace, uint32_t *status, cudaStream_t st, cudaError_t *err,
+                      uint64_t wait_ns, int32_t hold_stage);
 
 }  // namespace w4

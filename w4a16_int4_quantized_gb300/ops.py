@@ -47,6 +47,7 @@ SIGNATURES = [
     ("w4_linear_w8a16", _i32, [_vp, _vp, _vp, _vp, _i64, _i64, _i64, _vp, _sz, _u32, _vp]),
     ("w4_linear_q4_group", _i32, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i32, _vp, _sz, _u32, _vp]),
     ("w4_chain_q4", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, _vp]),
+    ("w4_chain_q4_test_timeout", _i32, [_vp, _i32, _vp, _i32, _i32, _i32, _vp, _sz, C.c_uint64, _i32, _vp]),
     ("w4_chain_workspace_bytes", _sz, [_vp, _i32, _i32]),
     ("w4_pack_interleaved_n64", _i32, [_vp, _vp, _i64, _i64, _vp]),
     ("w4_pack_block32", _i32, [_vp, _vp, _vp, _i64, _i64, _vp]),
@@ -282,6 +283,20 @@ def chain_q4(x0, linears, passes: int, pass_output: int, workspace=None, stream=
     _check(raw.w4_chain_q4(_ptr(x0), x0.numel(), arr, len(linears), passes, pass_output, _ptr(workspace),
                            workspace.numel(), _stream(stream)), "w4_chain_q4")
     return [y for _, _, y, _ in linears]
+
+
+def chain_q4_test_timeout(x0, linears, passes: int, pass_output: int, wait_limit_ns: int, hold_stage: int,
+                          workspace=None, stream=None) -> int:
+    """w4_chain_q4_test_timeout: the chain with a short wait limit and,
+    hold_stage >= 0, one stage whose outputs are never published.  Returns
+    the call's status (the device status word reports the timeout)."""
+    arr = chain_descriptors(linears)
+    need = raw.w4_chain_workspace_bytes(arr, len(linears), x0.numel())
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x0.device)
+    return raw.w4_chain_q4_test_timeout(_ptr(x0), x0.numel(), arr, len(linears), passes, pass_output,
+                                        _ptr(workspace), workspace.numel(), int(wait_limit_ns), int(hold_stage),
+                                        _stream(stream))
 
 
 def pack_interleaved_n64(w: torch.Tensor, K: int, stream=None) -> torch.Tensor:
