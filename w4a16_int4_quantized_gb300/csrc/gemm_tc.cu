@@ -162,16 +162,27 @@ W4_DEV bool wait_or_abort(uint64_t *bar, uint32_t parity, Smem *sh, uint32_t *st
 // ---------------------------------------------------------------- weight conversion
 
 // 8 packed signed nibbles (columns c..c+7) -> 8 bf16 = bf16_rne(q * s), as 16 bytes.
+// u' = u ^ 8 = q + 8 of each nibble goes under the exponent byte 0x4B by one
+// PRMT (the float 2^23 + u', exact); q * s = (that - (2^23 + 8)) * s is
+// exact in f32, formed two columns at a time with packed f32x2 arithmetic,
+// and rounded once to bf16.
 W4_DEV uint4 conv_w4a16(uint32_t w, float s) {
+    const uint32_t v = w ^ 0x88888888u;
+    const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        const uint32_t lo = (w >> (8 * e)) & 0xFu, hi = (w >> (8 * e + 4)) & 0xFu;
-        // 2^23 + (u ^ 8) = 2^23 + 8 + q exactly; subtracting 2^23 + 8 leaves q
-        const float ql = __int_as_float(0x4B000000 | (lo ^ 8u)) - 8388616.0f;
-        const float qh = __int_as_float(0x4B000000 | (hi ^ 8u)) - 8388616.0f;
-        __nv_bfloat162 b = __floats2bfloat162_rn(ql * s, qh * s);
-        o[e] = *reinterpret_cast<uint32_t *>(&b);
+        const uint32_t fl = prmt(lo, 0x4B000000u, 0x7540u | e), fh = prmt(hi, 0x4B000000u, 0x7540u | e);
+        asm("{\n\t.reg .b64 v, c, m, r;\n\t.reg .f32 r0, r1;\n\t"
+            "mov.b64 v, {%1, %2};\n\t"
+            "mov.b64 c, {%3, %3};\n\t"
+            "mov.b64 m, {%4, %4};\n\t"
+            "add.rn.f32x2 r, v, c;\n\t"
+            "mul.rn.f32x2 r, r, m;\n\t"
+            "mov.b64 {r0, r1}, r;\n\t"
+            "cvt.rn.bf16x2.f32 %0, r1, r0;\n\t}"
+            : "=r"(o[e])
+            : "r"(fl), "r"(fh), "f"(-8388616.0f), "f"(s));
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
