@@ -62,6 +62,7 @@ constexpr int kTmemCols = 512;  // two accumulators of kBN columns
 struct GemmParams {
     CUtensorMap xmap;  // 16-bit activations [M][Kx], box {64, 256}, 128B swizzle
     CUtensorMap wmap;  // packed weights [N][Kb] bytes, box {32|64, 128}
+    CUtensorMap smap;  // W4A16 row-major, s_tma: f16 scales [N][ng], box {8 groups, 128 rows}
     const uint16_t *scales;  // W4A16, W4A8G: f16 [N][ng]
     const uint8_t *zeros;    // W4A8G: zero points [N][ng]
     const float *sx;         // int kinds: [M]
@@ -69,13 +70,15 @@ struct GemmParams {
     float *y;                // [M][N]
     uint32_t *status;
     int M, N, K, G, ng;
+    int s_tma;  // the group scales of each stage arrive by TMA with the packed weights
     int nk;   // k-blocks of 64 columns
     int ntn;  // tiles along N (n fastest)
     int ntiles;
 };
 
 struct Smem {
-    uint64_t tma_full[kStages];
+    uint64_t tma_full[kStages];  // the activation tile of a stage
+    uint64_t w_full[kStages];    // the packed weight tile (and its group scales) of a stage
     uint64_t conv_full[kStages];
     uint64_t empty[kStages];
     uint64_t acc_full[2];
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     constexpr int kATile = kBM * 128;                // 16 KB
     constexpr int kBTile = kBN * 128;                // 32 KB
     constexpr int kPTile = kBM * kPRow;              // 4 | 8 KB
-    constexpr uint32_t kStageTx = kBTile + kPTile;
+    constexpr uint32_t kSTile = kBM * 16;                // 2 KB: 8 f16 group scales per weight row
     constexpr uint32_t kIdesc = idesc_f16((KIND == KIND_W4A16 || KIND == KIND_W8A16) ? 1u : 0u, kBM, kBN);
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -273,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     uint8_t *a_tiles = smem + 1024;
     uint8_t *b_tiles = a_tiles + kStages * kATile;
     uint8_t *p_tiles = b_tiles + kStages * kBTile;
+    uint8_t *s_tiles = p_tiles + kStages * kPTile;  // s_tma: [stage][128 rows][8 f16 scales]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...; tile t -> (n-tile t % ntn, m-tile t / ntn)
@@ -286,6 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sh->tma_full[s], 1);
+            mbar_init(&sh->w_full[s], 1);
             mbar_init(&sh->conv_full[s], 32 * kConvWarps);
             mbar_init(&sh->empty[s], 1);
         }
@@ -311,10 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 int m0, n0;
                 tile_of(g / p.nk, m0, n0);
                 if (g >= kStages && !wait_or_abort(&sh->empty[s], ((g / kStages) - 1) & 1, sh, p.status)) break;
-                mbar_arrive_expect_tx(&sh->tma_full[s], kStageTx);
+                // the weights first: the converters need them before the MMA needs the activations
+                mbar_arrive_expect_tx(&sh->w_full[s], kPTile + (p.s_tma ? kSTile : 0u));
+                if constexpr (IL) tma_load_3d(p_tiles + s * kPTile, &p.wmap, 0, kb * kBK, n0 / 64, &sh->w_full[s]);
+                else tma_load_2d(p_tiles + s * kPTile, &p.wmap, kb * kPRow, n0, &sh->w_full[s]);
+                if (p.s_tma)
+                    tma_load_2d(s_tiles + s * kSTile, &p.smap, (kb * kBK / p.G) & ~7, n0, &sh->w_full[s]);
+                mbar_arrive_expect_tx(&sh->tma_full[s], kBTile);
                 tma_load_2d(b_tiles + s * kBTile, &p.xmap, kb * kBK, m0, &sh->tma_full[s]);
-                if constexpr (IL) tma_load_3d(p_tiles + s * kPTile, &p.wmap, 0, kb * kBK, n0 / 64, &sh->tma_full[s]);
-                else tma_load_2d(p_tiles + s * kPTile, &p.wmap, kb * kPRow, n0, &sh->tma_full[s]);
             }
         }
     } else if (warp == 1) {
@@ -384,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         for (int g = 0; g < total; ++g) {
             const int s = g % kStages;
             if (g + 1 < total) load_il_scales(g + 1, s_nxt);
-            if (!wait_or_abort(&sh->tma_full[s], (g / kStages) & 1, sh, p.status)) break;
+            if (!wait_or_abort(&sh->w_full[s], (g / kStages) & 1, sh, p.status)) break;
             uint32_t lo[4], hi[4];
             deinterleave8(p_tiles + s * kPTile + ib * 2048 + k8 * 8 * 32, dq, lo, hi);
 #pragma unroll
@@ -446,12 +455,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
             }
         };
-        if (total > 0) load_scales(0, sc_cur);
+        if (total > 0 && !p.s_tma) load_scales(0, sc_cur);
         zb_cur = zb_nxt;
         for (int g = 0; g < total; ++g) {
             const int s = g % kStages;
-            if (g + 1 < total) load_scales(g + 1, sc_nxt);
-            if (!wait_or_abort(&sh->tma_full[s], (g / kStages) & 1, sh, p.status)) break;
+            if (g + 1 < total && !p.s_tma) load_scales(g + 1, sc_nxt);
+            if (!wait_or_abort(&sh->w_full[s], (g / kStages) & 1, sh, p.status)) break;
+            if (KIND == KIND_W4A16 && p.s_tma) {
+                // the stage's scales came with its weights: one group for the thread's
+                // 32 columns (G is a multiple of 32), at its place in the 8-group box
+                const int c0 = (g % p.nk) * kBK;
+                const int gi = (c0 + 32 * half) / p.G - ((c0 / p.G) & ~7);
+                const float sv = __half2float(__ushort_as_half(
+                    *reinterpret_cast<const uint16_t *>(s_tiles + s * kSTile + row * 16 + 2 * gi)));
+#pragma unroll
+                for (int c = 0; c < 4; ++c) sc_cur[c] = sv;
+            }
             const uint8_t *prow = p_tiles + s * kPTile + row * kPRow;
             uint8_t *arow = a_row + s * kATile;
             if constexpr (!kW4) {
@@ -580,7 +599,10 @@ __global__ void f32_to_bf16_kernel(const float *__restrict__ x, uint16_t *__rest
 }
 
 constexpr int smem_bytes(int kind) {
-    return 1024 + kStages * (kBM * 128 + kBN * 128 + kBM * ((kind == KIND_W8A8 || kind == KIND_W8A16) ? 64 : 32)) + 1024;
+    return 1024 +
+           kStages * (kBM * 128 + kBN * 128 + kBM * ((kind == KIND_W8A8 || kind == KIND_W8A16) ? 64 : 32) +
+                      (kind == KIND_W4A16 ? kBM * 16 : 0)) +
+           1024;
 }
 
 template <int KIND, bool IL>
@@ -698,6 +720,19 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
         if (!encode_tmap(&p.wmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.w, dims, strides, box,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
+    }
+    // W4A16 row-major: each stage's group scales by TMA beside its weights
+    // (8 groups x 128 rows per box; rows of whole 16-byte multiples).
+    p.s_tma = 0;
+    if (a.kind == KIND_W4A16 && !il && a.G % 32 == 0 && p.ng % 8 == 0 &&
+        reinterpret_cast<uintptr_t>(a.scale) % 16 == 0) {
+        const uint64_t dims[2] = {(uint64_t)p.ng, (uint64_t)a.N};
+        const uint64_t strides[1] = {(uint64_t)p.ng * 2};
+        const uint32_t box[2] = {8, (uint32_t)kBM};
+        if (!encode_tmap(&p.smap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, a.scale, dims, strides, box,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        p.s_tma = 1;
     }
     switch (a.kind) {
         case KIND_W4A16: return il ? launch_kernel<KIND_W4A16, true>(p, st) : launch_kernel<KIND_W4A16, false>(p, st);
