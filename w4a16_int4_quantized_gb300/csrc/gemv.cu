@@ -2584,8 +2584,9 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     {
         GemvParams q = p;
         int rb = 0, nrbw = 0, sthreads = 0, ssmem = 0;
-        if (pdl && a.kind == KIND_W4A16 && S == 1 && plan_stream(a, q, rb, nrbw, sthreads, ssmem) &&
-            ceil_div(a.N, (int64_t)q.R) >= 120) {
+        if (pdl && (a.kind == KIND_W4A16 || a.kind == KIND_W4A8) && S == 1 &&
+            plan_stream(a, q, rb, nrbw, sthreads, ssmem) && ceil_div(a.N, (int64_t)q.R) >= 120) {
+            if (a.kind == KIND_W4A8) return dispatch_stream<KIND_W4A8, 1>(q, rb, nrbw, sthreads, ssmem, st, pdl);
             switch (p.cpg) {
                 case 1: return dispatch_stream<KIND_W4A16, 1>(q, rb, nrbw, sthreads, ssmem, st, pdl);
                 case 4: return dispatch_stream<KIND_W4A16, 4>(q, rb, nrbw, sthreads, ssmem, st, pdl);
