@@ -421,6 +421,8 @@ class Workload:
             return 1 + (1 if self.ws is not None else 0)  # (f32 -> bf16 prepass), linear
         if w["kind"] == "w4a8" and w["M"] == 1 and w["layout"] == 0 and w["N"] >= 1024:
             return 1  # the rows are quantised inside the linear
+        if w["kind"] == "w4a8" and w["M"] > 16 and w["K"] % 8 == 0:
+            return 2  # quantizer (codes and their f16 image), GEMM
         return 2 + (1 if self.ws is not None else 0)  # quantize, (int8 -> f16 prepass), linear
 
     def kernel(self, i: int, flags: int = 1):

@@ -61,11 +61,28 @@ def test_linear_q4_f32_bitexact(ops, ora, flags, M, N, K):
     check(ops, ora, x, W, flags=flags)
 
 
-@pytest.mark.parametrize("M", [9, 16, 40])
+@pytest.mark.parametrize("M", [9, 16, 40, 300, 2048])
 def test_linear_q4_f32_batches(ops, ora, M):
     x = synth.activations_f32(161 + M, M, 2048)
-    W = synth.weights_f32(162, 2048, 2048)
+    W = synth.weights_f32(162, 2048 if M <= 300 else 384, 2048)
     check(ops, ora, x, W, flags=1)
+
+
+@pytest.mark.parametrize("K", [8, 1024, 2056, 4096])
+def test_linear_q4_f32_prefill_rows(ops, ora, K):
+    """M > 16: one pass quantises the rows and writes the f16 image the
+    tensor-core GEMM reads; rows of at most 2048 columns stay in registers,
+    longer rows are read twice.  Row 0 holds exact ties, row 1 is zero,
+    row 2 has a tiny amax (the reciprocal of the scale overflows)."""
+    M = 40
+    x = synth.activations_f32(165 + K, M, K)
+    x[0, :] = (np.arange(K) % 254 - 127).astype(np.float32) + 0.5
+    x[0, 0] = 127.0
+    x[1, :] = 0.0
+    x[2, :] = np.float32(1e-40) * ((np.arange(K) % 5) - 2)
+    W = synth.weights_f32(166 + K, 256, K)
+    check(ops, ora, x, W, flags=1)
+    check(ops, ora, x, synth.weights_f32(167 + K, 256, K), flags=1, layout=ops.LAYOUT_N64)
 
 
 def test_linear_q4_f32_interleaved(ops, ora):

@@ -182,6 +182,16 @@ w4_status w4_linear_q4_f32(const float *x, const uint8_t *w, const float *sw, fl
         a.xf = x; a.xq_out = xq; a.sx_out = sx;
         return cuda_status(w4::launch_gemv(a, st));  // fused, or the quantizer then the linear
     }
+    // Prefill on the tensor cores: one pass writes the codes, the scales and
+    // the f16 image of the codes the GEMM reads (no separate prepass).
+    if (N > 0 && K > 0 && M > 16 && K % 8 == 0 && w4::gemm_supported(a) &&
+        reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(xq) % 4 == 0 &&
+        reinterpret_cast<uintptr_t>(workspace) % 16 == 0) {
+        const cudaError_t e = w4::launch_quantize_rows_f16(x, M, K, xq, sx, static_cast<uint16_t *>(workspace), st);
+        if (e != cudaSuccess) return cuda_status(e);
+        a.x16_ready = true;
+        return run_linear(a, st);
+    }
     const cudaError_t e = w4::launch_quantize_rows(x, M, K, 127, xq, sx, nullptr, st);
     if (e != cudaSuccess) return cuda_status(e);
     if (N == 0) return W4_OK;

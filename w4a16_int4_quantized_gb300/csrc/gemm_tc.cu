@@ -680,7 +680,9 @@ cudaError_t launch_gemm(const LinearArgs &a, cudaStream_t st) {
         if (!a.workspace || a.ws_bytes < need) return cudaErrorInvalidValue;
         const int64_t groups = a.M * (Kx / 8);
         const int64_t blocks = std::min<int64_t>(ceil_div(groups, 256), 152 * 8);
-        if (a.kind == KIND_W8A16)  // f32 activations -> bf16 (the prefill's one rounding of x)
+        if (a.x16_ready)  // the row quantizer already wrote the f16 image
+            ;
+        else if (a.kind == KIND_W8A16)  // f32 activations -> bf16 (the prefill's one rounding of x)
             f32_to_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const float *>(a.x),
                                                                  static_cast<uint16_t *>(a.workspace), a.M, a.K, Kx);
         else

@@ -35,6 +35,8 @@ struct LinearArgs {
     const float *xf;
     int8_t *xq_out;
     float *sx_out;
+    // prefill of the int kinds: the workspace already holds the f16 image of the activation codes
+    bool x16_ready;
 };
 
 // capi.cu -- W4_OK for cudaSuccess; otherwise records e for w4_last_cuda_error and returns W4_ECUDA.
@@ -49,6 +51,9 @@ cudaError_t launch_quantize_rows(const float *x, int64_t rows, int64_t K, int Q,
                                  int32_t *rowsum, cudaStream_t st);
 cudaError_t launch_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw,
                                       cudaStream_t st);
+// quantize_row_q8 of M rows (K % 8 == 0) plus the f16 image of the codes, [M][K], for the prefill GEMM.
+cudaError_t launch_quantize_rows_f16(const float *x, int64_t M, int64_t K, int8_t *q, float *s, uint16_t *xh,
+                                     cudaStream_t st);
 cudaError_t launch_dot_i32_q4(const int8_t *xq, const uint8_t *wrow, int64_t K, int32_t *out, cudaStream_t st);
 cudaError_t launch_pack_n64(const uint8_t *w, uint8_t *il, int64_t N, int64_t K, cudaStream_t st);
 cudaError_t launch_pack_block32(const uint8_t *w, const uint16_t *s, uint8_t *blocks, int64_t N, int64_t K,

@@ -8,6 +8,8 @@
 // kernels use __fdiv_rn and __float2int_rn (IEEE round-to-nearest-even) and
 // max via fmaxf, which is exact and order-free, so their codes and scales
 // are bit-identical to the CPU definition.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -96,6 +98,83 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *__
     }
 }
 
+// quantize_row_q8 for the prefill path, one warp per row, and the exact f16
+// image of the codes that the tensor-core GEMM reads (its activation
+// operand), in the same pass.  K % 8 == 0.  Rows of up to 2048 columns stay
+// in registers (16 four-column vectors per lane); longer rows are read a
+// second time for the codes.  Codes are clamp(rint(fl(v / sx)), -127, 127)
+// with sx = fl(amax / 127): t = fl(v * fl(1 / sx)) lies within 2^-15 of
+// fl(v / sx) when |v / sx| < 256, so rint(t) decides unless t is within
+// 2^-13 of a half-integer, where the IEEE quotient is taken (and for every
+// value when 1 / sx overflows).
+constexpr int kQF16Warps = 8;
+constexpr int kQF16Vec = 16;  // float4 per lane held in registers
+
+W4_DEV int code_of(float v, float sx, float r, bool fast) {
+    if (sx == 0.0f) return 0;
+    const float t = __fmul_rn(v, r);
+    const float rt = rintf(t);
+    const int c = (fast && fabsf(t) < 256.0f && 0.5f - fabsf(t - rt) > 0x1p-13f) ? __float2int_rn(rt)
+                                                                                  : __float2int_rn(__fdiv_rn(v, sx));
+    return min(max(c, -127), 127);
+}
+
+W4_DEV void store_codes(int8_t *qr, uint16_t *hr, int k, const float4 &v, float sx, float r, bool fast) {
+    const int c0 = code_of(v.x, sx, r, fast), c1 = code_of(v.y, sx, r, fast);
+    const int c2 = code_of(v.z, sx, r, fast), c3 = code_of(v.w, sx, r, fast);
+    *reinterpret_cast<uint32_t *>(qr + k) = (uint32_t)(uint8_t)c0 | ((uint32_t)(uint8_t)c1 << 8) |
+                                            ((uint32_t)(uint8_t)c2 << 16) | ((uint32_t)(uint8_t)c3 << 24);
+    const uint32_t h0 = __half_as_ushort(__int2half_rn(c0)), h1 = __half_as_ushort(__int2half_rn(c1));
+    const uint32_t h2 = __half_as_ushort(__int2half_rn(c2)), h3 = __half_as_ushort(__int2half_rn(c3));
+    *reinterpret_cast<uint2 *>(hr + k) = make_uint2(h0 | (h1 << 16), h2 | (h3 << 16));
+}
+
+__global__ void __launch_bounds__(32 * kQF16Warps) quantize_rows_f16_kernel(const float *__restrict__ x, int64_t M,
+                                                                            int64_t K, int8_t *__restrict__ q,
+                                                                            float *__restrict__ s,
+                                                                            uint16_t *__restrict__ xh) {
+    griddep_launch_dependents();
+    griddep_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * kQF16Warps + (threadIdx.x >> 5);
+    if (row >= M) return;
+    const float4 *xr = reinterpret_cast<const float4 *>(x + row * K);
+    const int n4 = (int)(K >> 2);
+    const bool regs = n4 <= 32 * kQF16Vec;
+    float4 v[kQF16Vec];
+    float amax = 0.0f;
+    if (regs) {
+#pragma unroll
+        for (int i = 0; i < kQF16Vec; ++i) {
+            const int j = lane + 32 * i;
+            v[i] = j < n4 ? __ldg(xr + j) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[i].x), fabsf(v[i].y)), fmaxf(fabsf(v[i].z), fabsf(v[i].w))));
+        }
+    } else {
+        for (int j = lane; j < n4; j += 32) {
+            const float4 a = __ldg(xr + j);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sx = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) s[row] = sx;
+    const float r = sx != 0.0f ? __frcp_rn(sx) : 0.0f;
+    const bool fast = isfinite(r);
+    int8_t *qr = q + row * K;
+    uint16_t *hr = xh + row * K;
+    if (regs) {
+#pragma unroll
+        for (int i = 0; i < kQF16Vec; ++i) {
+            const int j = lane + 32 * i;
+            if (j < n4) store_codes(qr, hr, 4 * j, v[i], sx, r, fast);
+        }
+    } else {
+        for (int j = lane; j < n4; j += 32) store_codes(qr, hr, 4 * j, __ldg(xr + j), sx, r, fast);
+    }
+}
+
 // One CTA per output channel: Q4 codes stored u = q + 8, two per byte, low
 // nibble = even column; odd K pads the last high nibble with 8.
 __global__ void __launch_bounds__(kThreads) quantize_q4_kernel(const float *__restrict__ W, int64_t K,
@@ -170,6 +249,21 @@ cudaError_t launch_quantize_rows(const float *x, int64_t rows, int64_t K, int Q,
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, quantize_rows_kernel, x, K, Q, q, s, rowsum);
+}
+
+cudaError_t launch_quantize_rows_f16(const float *x, int64_t M, int64_t K, int8_t *q, float *s, uint16_t *xh,
+                                     cudaStream_t st) {
+    if (K % 8 != 0 || M > 0x3FFFFFFF) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ceil_div(M, kQF16Warps), 1, 1);
+    cfg.blockDim = dim3(32 * kQF16Warps, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_rows_f16_kernel, x, M, K, q, s, xh);
 }
 
 cudaError_t launch_quantize_matrix_q4(const float *W, int64_t N, int64_t K, uint8_t *packed, float *sw,
