@@ -41,3 +41,34 @@ def test_reference_arm_line():
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_extra_lines_cover_the_benchmark_set():
+    """The default run's extra lines: every decode-grid and prefill workload exists."""
+    for name in bench.EXTRA_DECODE + bench.EXTRA_PREFILL:
+        assert name in bench.WORKLOADS, name
+    grid = {(w["kind"], w["M"], w["N"], w["layout"]) for n in bench.EXTRA_DECODE
+            for w in [bench.WORKLOADS[n]] if n.startswith(("w4a16_decode", "w4a8_decode"))}
+    for kind in ("w4a16", "w4a8"):
+        for M in (1, 4, 16):
+            for N in (13312, 3072):
+                for lay in (0, 1):
+                    assert (kind, M, N, lay) in grid, (kind, M, N, lay)
+    pre = {(bench.WORKLOADS[n]["kind"], bench.WORKLOADS[n]["N"]) for n in bench.EXTRA_PREFILL}
+    assert {(k, n) for k in ("w4a8", "w4a16") for n in (2048, 3072, 13312)} <= pre
+
+
+def test_reference_arm_bounded_for_many_steps():
+    """Many steps with a tiny budget: each step samples output channels
+    instead of whole calls, so the run ends quickly and says so."""
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps",
+                          "20000", "--warmup", "1", "--cpu-seconds", "0.5"], capture_output=True, text=True,
+                         timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["steps"] == 20000 and line["value"] > 0
+    assert "output channels sampled" in line["cpu_baseline"]["sample"]
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
