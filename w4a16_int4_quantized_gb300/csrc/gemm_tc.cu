@@ -514,14 +514,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const int b = i & 1;
             int m0, n0;
             tile_of(i, m0, n0);
-            bool ok = wait_or_abort(&sh->acc_full[b], (i >> 1) & 1, sh, p.status);
-            ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
-            if (!ok) break;
-            tc_fence_after();
+            // the tile's scales, loaded while its accumulator is still being formed
             const int nrow = n0 + 32 * q + lane;
             float swn = 1.0f;
             if constexpr (KIND == KIND_W4A8 || KIND == KIND_W8A8 || KIND == KIND_W8A16)
                 swn = (nrow < p.N) ? p.sw[nrow] : 0.0f;
+            float sx_pre[kBN / 64];
+#pragma unroll
+            for (int cc = 0; cc < kBN / 64; ++cc) {
+                const int mm = m0 + (kBN / 2) * hc + 32 * cc + lane;
+                sx_pre[cc] = 0.0f;
+                if constexpr (KIND != KIND_W4A16 && KIND != KIND_W8A16) sx_pre[cc] = mm < p.M ? p.sx[mm] : 0.0f;
+            }
+            bool ok = wait_or_abort(&sh->acc_full[b], (i >> 1) & 1, sh, p.status);
+            ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < kBN / 64; ++cc) {
                 const int col0 = (kBN / 2) * hc + 32 * cc;
@@ -533,10 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sh->acc_empty[b]);
                 }
-                // sx of the chunk's 32 activation rows: one coalesced load, then shuffles
-                float sxl = 0.0f;
-                if constexpr (KIND != KIND_W4A16 && KIND != KIND_W8A16)
-                    sxl = (m0 + col0 + lane < p.M) ? p.sx[m0 + col0 + lane] : 0.0f;
+                // sx of the chunk's 32 activation rows (loaded above), then shuffles
+                static_assert(kBN / 64 == 4, "four 32-column chunks per epilogue warp");
+                const float sxl = cc == 0 ? sx_pre[0] : cc == 1 ? sx_pre[1] : cc == 2 ? sx_pre[2] : sx_pre[3];
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {  // every lane takes part in the shuffles
                     const int m = m0 + col0 + j;
