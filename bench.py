@@ -121,8 +121,14 @@ EXTRA_PREFILL = ([f"{k}_prefill_m2048_n{n}" for k in ("w4a8", "w4a16") for n in 
 # capture of that kernel on that workload; None where no capture matches the
 # current kernel.
 TRAFFIC = {
-    "w4a16_gemv_m1": 2393856,                 # streaming W4A16 GEMV, M=1, N=K=2048, G=32
-    "w4a8_gemv_m1": 2141184,                  # fused quantize + W4A8 dp4a GEMV, M=1, N=K=2048
+    "w4a16_gemv_m1": 2391552,                 # all-warp W4A16 GEMV, M=1, N=K=2048, G=32
+    "w4a8_gemv_m1": 2137600,                  # all-warp fused quantize + W4A8 dp4a GEMV, M=1, N=K=2048
+    "w4a16_decode_m1_n13312": 14088448,       # all-warp W4A16 GEMV, M=1, N=13312, G=128
+    "w4a16_decode_m16_n13312": 14181376,      # streaming W4A16 GEMV, two activation tiles
+    "w4a16_decode_m1_n13312_il": 14097664,    # staged W4A16 GEMV from the interleaved layout
+    "w4a8g_decode_m1_n13312": 14320640,       # staged grouped W4A8 GEMV
+    "w8a16_decode_m1_n13312": 27356416,       # staged W8A16 GEMV
+    "w4a16_b32_decode_m1_n13312": 15372544,   # staged W4A16 GEMV on inline-scale blocks
 }
 
 
