@@ -366,3 +366,23 @@ def test_pdl_flag_same_bits(ops, ora):
 def test_device_status_clean(ops):
     torch.cuda.synchronize()
     assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("N,G", [(13312, 128), (7680, 32), (8192, 64)])
+def test_w4a16_interleaved_m1_pdl_same_bits(ops, ora, N, G):
+    """M = 1 under PDL from the interleaved [N/64][K][32 B] layout: the
+    all-warp kernel turns each 64-channel block into row-major rows in shared
+    memory, so the result equals the row-major call bit for bit (and G = 64
+    takes the staged kernel, also bit-identical).  Sampled rows against the oracle."""
+    K = 2048
+    x, w, s = synth.w4a16_inputs(171 + N + G, 1, N, K, G)
+    xd, wd, sd = dev(x), dev(w), dev(s)
+    y0 = host(ops.linear_w4a16_group(xd, wd, sd, G, K=K))
+    wil = ops.pack_interleaved_n64(wd, K)
+    y1 = host(ops.linear_w4a16_group(xd, wil, sd, G, K=K, N=N, layout=ops.LAYOUT_N64, flags=ops.FLAG_PDL))
+    y2 = host(ops.linear_w4a16_group(xd, wil, sd, G, K=K, N=N, layout=ops.LAYOUT_N64))
+    assert np.array_equal(bits(y1), bits(y0))
+    assert np.array_equal(bits(y2), bits(y0))
+    rows = np.sort(np.random.default_rng(N).choice(N, 128, replace=False))
+    w4a16_check(np.ascontiguousarray(y1[:, rows]), ora, x, w[rows], s[rows], K, G)
+    assert ops.device_status() == 0

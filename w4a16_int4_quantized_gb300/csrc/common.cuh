@@ -183,10 +183,8 @@ W4_DEV uint4 lds_u128(uint32_t addr) {
 // [k][32 B] (byte d = channel d | channel d+32 << 4) of 8 consecutive k for
 // channels 4*dq..4*dq+3 -> one packed row-major word (8 nibbles, low first)
 // for each of the channels 4*dq+c (lo[c]) and 4*dq+c+32 (hi[c]).
-W4_DEV void deinterleave8(const uint8_t *raw, int dq, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
-    uint32_t v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint32_t *>(raw + i * 32 + 4 * dq);
+// The same, from the 8 words (bytes 4dq..4dq+3 of the 8 rows) already in registers.
+W4_DEV void deinterleave8_words(const uint32_t (&v)[8], uint32_t (&lo)[4], uint32_t (&hi)[4]) {
     uint32_t T[2][4];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -206,6 +204,13 @@ W4_DEV void deinterleave8(const uint8_t *raw, int dq, uint32_t (&lo)[4], uint32_
         lo[c] = prmt(la | (la >> 4), lb | (lb >> 4), 0x6420);
         hi[c] = prmt(ha | (ha >> 4), hb | (hb >> 4), 0x6420);
     }
+}
+
+W4_DEV void deinterleave8(const uint8_t *raw, int dq, uint32_t (&lo)[4], uint32_t (&hi)[4]) {
+    uint32_t v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint32_t *>(raw + i * 32 + 4 * dq);
+    deinterleave8_words(v, lo, hi);
 }
 
 W4_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }

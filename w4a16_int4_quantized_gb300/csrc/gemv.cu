@@ -1502,7 +1502,12 @@ __global__ void __launch_bounds__(512, 2) gemv_q4dp_kernel(const __grid_constant
 //    paths folds its units u = w', w' + WK, ... in order, acc = fma(s_u,
 //    part_u, acc), and the WK sums are added in index order -- bit for bit
 //    the result of every other M <= 16 path for the same (N, K, G).
-template <int CPG, int NU, int JJ>
+// IL: the weights are in the interleaved [N/64][K][32 B] layout and each CTA
+// owns one 64-channel block; before the wait its threads turn the block into
+// row-major rows in shared memory (4x4 byte transposes and nibble repacking,
+// the decode path's deinterleave), after which everything is as above, so
+// both layouts give the same bits.
+template <int CPG, int NU, int JJ, bool IL = false>
 __global__ void __launch_bounds__(512, 2) gemv_m1_w4a16_kernel(const __grid_constant__ GemvParams p) {
     griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1531,14 +1536,37 @@ __global__ void __launch_bounds__(512, 2) gemv_m1_w4a16_kernel(const __grid_cons
     if (warp == 0) {
         if (lane == 0) {
             for (int b = 0; b < nrb; ++b)
-                mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(16, rows - 16 * b) * (p.Kb + sbytes)));
+                mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(16, rows - 16 * b) * ((IL ? 0 : p.Kb) + sbytes)));
             prefetch_l2(p.x, (uint32_t)p.x_pref);
         }
         __syncwarp();
         const uint16_t *s16 = static_cast<const uint16_t *>(p.scale);
         for (int r = lane; r < rows; r += 32) {
-            bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb, &bars[r >> 4]);
+            if constexpr (!IL)
+                bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb,
+                         &bars[r >> 4]);
             bulk_g2s(smem + p.sc_off + r * sbytes, s16 + (size_t)(row0 + r) * p.ng, (uint32_t)sbytes, &bars[r >> 4]);
+        }
+    }
+    if constexpr (IL) {
+        // the block [K][32 B] -> row-major rows: task (dq, k8) reads bytes
+        // 4dq..4dq+3 of rows 8k8..8k8+7 and writes word k8 of channels
+        // 4dq..4dq+3 and 4dq+32..4dq+35 (K % 8 == 0, one block per CTA)
+        const uint8_t *raw = p.w + (size_t)blockIdx.x * p.K * 32;
+        const int ntask = p.K;  // 8 quads x K / 8 column groups
+        for (int task = tid; task < ntask; task += nw * 32) {
+            const int dq = task & 7, k8 = task >> 3;
+            uint32_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = __ldg(reinterpret_cast<const uint32_t *>(raw + (size_t)(8 * k8 + i) * 32 + 4 * dq));
+            uint32_t lo[4], hi[4];
+            deinterleave8_words(v, lo, hi);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c) * p.wstride + 4 * k8) = lo[c];
+                *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c + 32) * p.wstride + 4 * k8) = hi[c];
+            }
         }
     }
 
@@ -2113,11 +2141,11 @@ cudaError_t launch_q4dp(const GemvParams &p, int threads, int smem, cudaStream_t
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int CPG, int NU, int JJ>
+template <int CPG, int NU, int JJ, bool IL = false>
 cudaError_t launch_m1_w4a16(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    auto *kern = gemv_m1_w4a16_kernel<CPG, NU, JJ>;
+    auto *kern = gemv_m1_w4a16_kernel<CPG, NU, JJ, IL>;
     std::call_once(once, [kern] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
@@ -2340,7 +2368,11 @@ bool plan_stream(const LinearArgs &a, GemvParams &p, int &rb_out, int &nrbw_out,
 // the call's WK.  Rows per CTA: a multiple of 8, spread over the fewest
 // waves of 152 CTAs, within two CTAs' worth of shared memory per SM.
 bool plan_m1_w4a16(const LinearArgs &a, GemvParams &p, int &threads, int &smem) {
-    if (a.kind != KIND_W4A16 || a.M != 1 || a.layout != W4_LAYOUT_ROWMAJOR || p.upc != p.units) return false;
+    const bool il = a.layout == W4_LAYOUT_N64;
+    if (a.kind != KIND_W4A16 || a.M != 1 || p.upc != p.units) return false;
+    if (a.layout != W4_LAYOUT_ROWMAJOR && !il) return false;
+    // interleaved: one 64-channel block per CTA, transposed from K % 8 == 0 rows
+    if (il && (a.K % 8 != 0 || a.N / 64 < 120)) return false;
     if (p.WK != 1 && p.WK != 2 && p.WK != 4) return false;
     if (p.Kb % 16 != 0 || (2 * p.ng) % 16 != 0 || reinterpret_cast<uintptr_t>(a.scale) % 16 != 0) return false;
     if (p.cpg != 1 && p.cpg != 2 && p.cpg != 4) return false;
@@ -2375,9 +2407,9 @@ bool plan_m1_w4a16(const LinearArgs &a, GemvParams &p, int &threads, int &smem) 
     };
     int rmax = 256;
     while (rmax >= 8 && layout(rmax) > cap) rmax -= 8;
-    if (rmax < 8) return false;
+    if (rmax < 8 || (il && rmax < 64)) return false;
     const int64_t waves = ceil_div(a.N, (int64_t)152 * rmax);
-    const int R = (int)std::min<int64_t>(rmax, round_up(ceil_div(a.N, 152 * waves), 8));
+    const int R = il ? 64 : (int)std::min<int64_t>(rmax, round_up(ceil_div(a.N, 152 * waves), 8));
     p.R = R;
     const int off = layout(R);
     threads = 32 * (chunks / nch);
@@ -2559,7 +2591,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
         }
     }
     // W4A16, M = 1, no K split, PDL: every warp of the CTA after the wait (same bits).
-    if (pdl && a.kind == KIND_W4A16 && a.M == 1 && S == 1 && a.N >= 1024) {
+    if (pdl && a.kind == KIND_W4A16 && a.M == 1 && S == 1 && a.N >= 1024 && a.layout != W4_LAYOUT_B32) {
         GemvParams q = p;
         q.WK = s.WK;
         q.upc = p.units;
@@ -2568,13 +2600,19 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
             // (chunks per unit, units per warp, units per fold chain)
             const int nu = (p.units * p.cpg > 64 ? 8 : 4) / p.cpg, jj = p.units / 4;
             cudaError_t (*fn)(const GemvParams &, int, int, cudaStream_t, bool) = nullptr;
-            if (p.cpg == 1 && nu == 4 && jj == 16) fn = launch_m1_w4a16<1, 4, 16>;
-            if (p.cpg == 1 && nu == 4 && jj == 8) fn = launch_m1_w4a16<1, 4, 8>;
-            if (p.cpg == 2 && nu == 2 && jj == 8) fn = launch_m1_w4a16<2, 2, 8>;
-            if (p.cpg == 2 && nu == 2 && jj == 4) fn = launch_m1_w4a16<2, 2, 4>;
-            if (p.cpg == 2 && nu == 4 && jj == 16) fn = launch_m1_w4a16<2, 4, 16>;
-            if (p.cpg == 4 && nu == 1 && jj == 4) fn = launch_m1_w4a16<4, 1, 4>;
-            if (p.cpg == 4 && nu == 2 && jj == 8) fn = launch_m1_w4a16<4, 2, 8>;
+            if (n64) {
+                // interleaved: the gate_up / down shapes of the decode set (G = 128 or 32)
+                if (p.cpg == 4 && nu == 1 && jj == 4) fn = launch_m1_w4a16<4, 1, 4, true>;
+                if (p.cpg == 1 && nu == 4 && jj == 16) fn = launch_m1_w4a16<1, 4, 16, true>;
+            } else {
+                if (p.cpg == 1 && nu == 4 && jj == 16) fn = launch_m1_w4a16<1, 4, 16>;
+                if (p.cpg == 1 && nu == 4 && jj == 8) fn = launch_m1_w4a16<1, 4, 8>;
+                if (p.cpg == 2 && nu == 2 && jj == 8) fn = launch_m1_w4a16<2, 2, 8>;
+                if (p.cpg == 2 && nu == 2 && jj == 4) fn = launch_m1_w4a16<2, 2, 4>;
+                if (p.cpg == 2 && nu == 4 && jj == 16) fn = launch_m1_w4a16<2, 4, 16>;
+                if (p.cpg == 4 && nu == 1 && jj == 4) fn = launch_m1_w4a16<4, 1, 4>;
+                if (p.cpg == 4 && nu == 2 && jj == 8) fn = launch_m1_w4a16<4, 2, 8>;
+            }
             if (fn) return fn(q, mthreads, msmem, st, pdl);
         }
     }
