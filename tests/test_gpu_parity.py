@@ -386,3 +386,19 @@ def test_w4a16_interleaved_m1_pdl_same_bits(ops, ora, N, G):
     rows = np.sort(np.random.default_rng(N).choice(N, 128, replace=False))
     w4a16_check(np.ascontiguousarray(y1[:, rows]), ora, x, w[rows], s[rows], K, G)
     assert ops.device_status() == 0
+
+
+@pytest.mark.parametrize("N", [13312, 7680])
+def test_linear_q4_interleaved_m1_pdl_bitexact(ops, ora, N):
+    """W4A8 at M = 1 under PDL from the interleaved layout (the all-warp
+    kernel transposes each 64-channel block in shared memory): the oracle's
+    bits, the same as the row-major call."""
+    K = 2048
+    x = synth.activations_f32(181 + N, 1, K)
+    W = synth.weights_f32(182 + N, N, K)
+    wq, sw = ora.quantize_matrix_q4(W)
+    xq, sx, _ = ora.quantize_row_q8(x)
+    wil = ops.pack_interleaved_n64(dev(wq), K)
+    y = host(ops.linear_q4(dev(xq), dev(sx), wil, dev(sw), K=K, N=N, layout=ops.LAYOUT_N64, flags=ops.FLAG_PDL))
+    assert np.array_equal(bits(y), bits(ora.linear_q4(xq, sx, wq, sw, K)))
+    assert ops.device_status() == 0

@@ -1733,7 +1733,10 @@ __global__ void __launch_bounds__(512, 2) gemv_m1_w4a16_kernel(const __grid_cons
 // codes and the scale out.  Then warp w takes rows w, w + 16, ...: each lane
 // dp4a's the low and high nibbles of its 16-byte chunks against the even and
 // odd codes.  The result is an exact integer, so any order gives the same bits.
-template <bool XQ, int CH>
+// IL: interleaved [N/64][K][32 B] weights, one 64-channel block per CTA,
+// turned into row-major rows in shared memory before the wait (as in
+// gemv_m1_w4a16_kernel); the nibbles are the same, so the sums are.
+template <bool XQ, int CH, bool IL = false>
 __global__ void __launch_bounds__(512, 2) gemv_m1_q4_kernel(const __grid_constant__ GemvParams p) {
     griddep_launch_dependents();
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1755,19 +1758,42 @@ __global__ void __launch_bounds__(512, 2) gemv_m1_q4_kernel(const __grid_constan
     __syncthreads();
     if (warp == 0) {
         if (lane == 0) {
-            for (int b = 0; b < nrb; ++b) mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(16, rows - 16 * b) * p.Kb));
+            if constexpr (!IL)
+                for (int b = 0; b < nrb; ++b)
+                    mbar_arrive_expect_tx(&bars[b], (uint32_t)(min(16, rows - 16 * b) * p.Kb));
             prefetch_l2(XQ ? static_cast<const void *>(p.xf) : p.x, (uint32_t)p.x_pref);
         }
         __syncwarp();
-        for (int r = lane; r < rows; r += 32)
-            bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb, &bars[r >> 4]);
+        if constexpr (!IL)
+            for (int r = lane; r < rows; r += 32)
+                bulk_g2s(smem + p.w_off + r * p.wstride, p.w + (size_t)(row0 + r) * p.Kb, (uint32_t)p.Kb,
+                         &bars[r >> 4]);
+    }
+    if constexpr (IL) {
+        // the block [K][32 B] -> row-major rows (K % 8 == 0, one block per CTA)
+        const uint8_t *raw = p.w + (size_t)blockIdx.x * p.K * 32;
+        for (int task = tid; task < p.K; task += nthr) {
+            const int dq = task & 7, k8 = task >> 3;
+            uint32_t v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                v[i] = __ldg(reinterpret_cast<const uint32_t *>(raw + (size_t)(8 * k8 + i) * 32 + 4 * dq));
+            uint32_t lo[4], hi[4];
+            deinterleave8_words(v, lo, hi);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c) * p.wstride + 4 * k8) = lo[c];
+                *reinterpret_cast<uint32_t *>(smem + p.w_off + (4 * dq + c + 32) * p.wstride + 4 * k8) = hi[c];
+            }
+        }
     }
     // one warp polls the copies, the others sleep in the CTA barrier
     bool ok = true;
-    if (warp == 0)
+    if (!IL && warp == 0)
         for (int b = 0; b < nrb; ++b) ok = mbar_wait_bounded(&bars[b], 0) && ok;
     __syncthreads();
-    for (int b = 0; b < nrb; ++b) ok = mbar_try_wait(&bars[b], 0) && ok;
+    if (!IL)
+        for (int b = 0; b < nrb; ++b) ok = mbar_try_wait(&bars[b], 0) && ok;
     uint4 w1[CH];  // the warp's first row
 #pragma unroll
     for (int i = 0; i < CH; ++i) {
@@ -1924,7 +1950,7 @@ __global__ void __launch_bounds__(512, 2) gemv_m1_q4_kernel(const __grid_constan
     }
     if (!ok) {
         if (lane == 0 && p.status) atomicOr(p.status, kStatusCopyTimeout);
-        for (int b = 0; b <= nrb; ++b) (void)mbar_wait_bounded(&bars[b], 0);
+        for (int b = IL ? nrb : 0; b <= nrb; ++b) (void)mbar_wait_bounded(&bars[b], 0);
     }
 }
 
@@ -2163,11 +2189,11 @@ cudaError_t launch_m1_w4a16(const GemvParams &p, int threads, int smem, cudaStre
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <bool XQ, int CH>
+template <bool XQ, int CH, bool IL = false>
 cudaError_t launch_m1_q4(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    auto *kern = gemv_m1_q4_kernel<XQ, CH>;
+    auto *kern = gemv_m1_q4_kernel<XQ, CH, IL>;
     std::call_once(once, [kern] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     });
@@ -2186,8 +2212,9 @@ cudaError_t launch_m1_q4(const GemvParams &p, int threads, int smem, cudaStream_
 }
 
 template <bool XQ>
-cudaError_t dispatch_m1_q4(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl) {
+cudaError_t dispatch_m1_q4(const GemvParams &p, int threads, int smem, cudaStream_t st, bool pdl, bool il = false) {
     const int chunks = p.Kb >> 4;
+    if (il) return launch_m1_q4<XQ, 2, true>(p, threads, smem, st, pdl);  // K = 2048: the planner allows only that
     if (chunks <= 32) return launch_m1_q4<XQ, 1>(p, threads, smem, st, pdl);
     if (chunks <= 64) return launch_m1_q4<XQ, 2>(p, threads, smem, st, pdl);
     return launch_m1_q4<XQ, 4>(p, threads, smem, st, pdl);
@@ -2420,7 +2447,11 @@ bool plan_m1_w4a16(const LinearArgs &a, GemvParams &p, int &threads, int &smem) 
 // Plans gemv_m1_q4_kernel (W4A8, M = 1, row-major, K <= 4096); false when it
 // does not apply.  xq: the fused call (f32 activations quantised in the CTAs).
 bool plan_m1_q4(const LinearArgs &a, GemvParams &p, bool xq, int &threads, int &smem) {
-    if (a.kind != KIND_W4A8 || a.M != 1 || a.layout != W4_LAYOUT_ROWMAJOR || a.N < 1024) return false;
+    const bool il = a.layout == W4_LAYOUT_N64;
+    if (a.kind != KIND_W4A8 || a.M != 1 || a.N < 1024) return false;
+    if (a.layout != W4_LAYOUT_ROWMAJOR && !il) return false;
+    // interleaved: one 64-channel block per CTA, K = 2048 (two chunks per lane), at least 120 blocks
+    if (il && (a.K != 2048 || a.N / 64 < 120)) return false;
     if (p.Kb % 16 != 0 || (p.Kb >> 4) > 128) return false;
     const void *x = xq ? static_cast<const void *>(a.xf) : a.x;
     if (reinterpret_cast<uintptr_t>(x) % 16 != 0) return false;
@@ -2429,7 +2460,7 @@ bool plan_m1_q4(const LinearArgs &a, GemvParams &p, bool xq, int &threads, int &
     p.wstride = pad_to(p.Kb, 16);
     p.x_pref = (int)((a.K * (xq ? 4 : 1)) & ~(int64_t)15);
     const int ncols = 2 * p.Kb;
-    const int R = (int)ceil_div(a.N, 152);
+    const int R = il ? 64 : (int)ceil_div(a.N, 152);
     int off = 0;
     p.bar_off = off;
     off += (int)round_up((ceil_div(R, 16) + 1) * 8, 128);
@@ -2532,7 +2563,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
             q.xf = a.xf;
             q.xq_out = a.xq_out;
             q.sx_out = a.sx_out;
-            return dispatch_m1_q4<true>(q, mthreads, msmem, st, (a.flags & W4_FLAG_PDL) != 0);
+            return dispatch_m1_q4<true>(q, mthreads, msmem, st, (a.flags & W4_FLAG_PDL) != 0, n64);
         }
         q = p;
         q.WK = s.WK;
@@ -2566,7 +2597,7 @@ cudaError_t launch_gemv(const LinearArgs &a, cudaStream_t st) {
     if (pdl && a.kind == KIND_W4A8 && a.M == 1) {
         GemvParams q = p;
         int mthreads = 0, msmem = 0;
-        if (plan_m1_q4(a, q, false, mthreads, msmem)) return dispatch_m1_q4<false>(q, mthreads, msmem, st, pdl);
+        if (plan_m1_q4(a, q, false, mthreads, msmem)) return dispatch_m1_q4<false>(q, mthreads, msmem, st, pdl, n64);
     }
     if (pdl && a.kind == KIND_W4A8 && a.M == 1 && a.layout == W4_LAYOUT_ROWMAJOR && S == 1 && (p.Kb >> 4) <= 128) {
         GemvParams q = p;
