@@ -142,6 +142,25 @@ def test_chain_validation(lib):
     assert r.w4_chain_workspace_bytes(None, 2, 64) == 0
 
 
+def test_chain_timeout_entry_validation(lib):
+    """The timeout test entry point checks its own two arguments first, then
+    the chain exactly as w4_chain_q4 does (passes = 0: nothing launches)."""
+    r = lib.raw
+    rows = [(96, 64, -1), (64, 96, 0)]
+    arr = (lib.ChainLinear * 2)(*[lib.ChainLinear(0x1000, 0x2000, 0x3000, N, K, inp, 0) for N, K, inp in rows])
+    ws = C.c_void_p(0x4000)
+    f = lambda wait_ns, hold, n=2, passes=0, K0=64: r.w4_chain_q4_test_timeout(
+        FAKE, K0, arr, n, passes, 1, ws, 1 << 20, wait_ns, hold, None)
+    assert f(1_000_000, -1) == lib.W4_OK
+    assert f(1_000_000, 7) == lib.W4_OK                   # no stage has index 7: nothing is held
+    assert f(1, -1) == lib.W4_OK and f(1_000_000_000, -1) == lib.W4_OK
+    assert f(0, -1) == lib.W4_EINVAL
+    assert f(1_000_000_001, -1) == lib.W4_EINVAL
+    assert f(1_000_000, -2) == lib.W4_EINVAL
+    assert f(1_000_000, -1, n=0) == lib.W4_EINVAL          # then the chain's own checks
+    assert f(1_000_000, -1, K0=48) == lib.W4_ESHAPE
+
+
 def test_linear_q4_group_validation(lib):
     r = lib.raw
     f = lambda M, N, K, G, layout=0, z=FAKE: r.w4_linear_q4_group(FAKE, FAKE, FAKE, FAKE, z, FAKE, M, N, K, G,
