@@ -39,6 +39,13 @@
  *   27 Q8 weight matrix row n quantised from row n - 1
  *   28 bf16 prefill dequantisation rounded through f16 instead
  *   29 bf16 prefill dequantisation truncated instead of rounded to even
+ *   30 inline-scale block stores its f16 scale big-endian
+ *   31 inline-scale reader takes the codes from the block's first byte
+ *   32 W8A16 codes read as unsigned bytes
+ *   33 int8 dot reads the second operand as unsigned
+ *   34 interleave reader swaps the two channels of a byte
+ *   35 interleave reader drops the odd-K pad nibble
+ *   36 W8A32 codes read as unsigned bytes
  * (s11, the missing NULL check, would crash the test process and is covered
  * by the host-side validation tests of the CUDA library instead.)
  */
@@ -265,7 +272,11 @@ int64_t ref_dot_naive_q4(const int8_t *xq, const uint8_t *wrow, int64_t K) {
 
 int32_t ref_dot_i32(const int8_t *a, const int8_t *b, int64_t K) {
     int32_t acc = 0;
+#if MUT(33)
+    for (int64_t k = 0; k < K; ++k) acc += (int32_t)a[k] * (int32_t)(uint8_t)b[k];
+#else
     for (int64_t k = 0; k < K; ++k) acc += (int32_t)a[k] * (int32_t)b[k];
+#endif
     return acc;
 }
 
@@ -345,7 +356,11 @@ int ref_linear_w8a16_exact(const float *x, const int8_t *wq, const float *sw, do
         for (int64_t n = 0; n < Nd; ++n) {
             double acc = 0.0, aacc = 0.0;
             for (int64_t k = 0; k < K; ++k) {
+#if MUT(32)
+                const double p = (double)x[m * K + k] * (double)(uint8_t)wq[n * K + k];
+#else
                 const double p = (double)x[m * K + k] * (double)wq[n * K + k];
+#endif
                 acc += p;
                 aacc += fabs(p);
             }
@@ -371,7 +386,11 @@ int ref_linear_w8a32(const float *x, const int8_t *wq, const float *s, float *y,
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < Nd; ++n) {
             float acc = 0.0f;
+#if MUT(36)
+            for (int64_t k = 0; k < K; ++k) acc = acc + x[m * K + k] * (float)(uint8_t)wq[n * K + k];
+#else
             for (int64_t k = 0; k < K; ++k) acc = acc + x[m * K + k] * (float)wq[n * K + k];
+#endif
 #if MUT(8)
             y[m * N + n] = acc;
 #elif MUT(7)
@@ -524,8 +543,13 @@ int ref_blocks_b32(const uint8_t *w, const uint16_t *s, uint8_t *blocks, int64_t
         for (int64_t b = 0; b < nb; ++b) {
             uint8_t *blk = blocks + (n * nb + b) * 18;
             const uint16_t sc = s[n * nb + b];
+#if MUT(30)
+            blk[0] = (uint8_t)(sc >> 8);
+            blk[1] = (uint8_t)(sc & 0xFF);
+#else
             blk[0] = (uint8_t)(sc & 0xFF);
             blk[1] = (uint8_t)(sc >> 8);
+#endif
             for (int64_t j = 0; j < 16; ++j) blk[2 + j] = w[n * Kb + 16 * b + j];
         }
     return REF_OK;
@@ -553,7 +577,11 @@ int ref_linear_w4a16_b32_exact(const uint16_t *x, const uint8_t *blocks, double 
                 for (int64_t i = 0; i < 32; ++i) {
                     const int64_t k = 32 * b + i;
                     if (k >= K) continue;
+#if MUT(31)
+                    const double p = (double)act_bf16(x[m * K + k]) * (double)ref_nibble_signed(nib(blk, i));
+#else
                     const double p = (double)act_bf16(x[m * K + k]) * (double)ref_nibble_signed(nib(blk + 2, i));
+#endif
                     part += p;
                     apart += fabs(p);
                 }
@@ -702,12 +730,20 @@ int ref_unpack_interleaved_n64(const uint8_t *w_il, uint8_t *w_rm, int64_t N, in
         for (int64_t k = 0; k < K; ++k)
             for (int d = 0; d < 32; ++d) {
                 const uint8_t byte = w_il[(b * K + k) * 32 + d];
+#if MUT(34)
+                const int64_t n0 = 64 * b + d + 32, n1 = 64 * b + d;
+#else
                 const int64_t n0 = 64 * b + d, n1 = 64 * b + d + 32;
+#endif
                 const unsigned sh = (unsigned)(k & 1) * 4u;
                 w_rm[n0 * Kb + k / 2] |= (uint8_t)((byte & 0xFu) << sh);
                 w_rm[n1 * Kb + k / 2] |= (uint8_t)((byte >> 4) << sh);
             }
+#if MUT(35)
+    (void)pad;
+#else
     if (K & 1)
         for (int64_t n = 0; n < N; ++n) w_rm[n * Kb + Kb - 1] |= (uint8_t)((pad & 0xFu) << 4);
+#endif
     return REF_OK;
 }

@@ -9,7 +9,8 @@ import pytest
 
 from tests import oracle_pins
 
-MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24, 25, 26, 27, 28, 29]
+MUTANTS = [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 12, 13, 14, 15, 16, 17, 18, 19, 20, 21, 22, 23, 24, 25, 26, 27, 28, 29,
+           30, 31, 32, 33, 34, 35, 36]
 # pins too slow to repeat for every mutant, and not needed to kill any of them
 _SKIP = {"f16_bruteforce", "bf16"}
 
