@@ -1037,6 +1037,21 @@ def microdecoder_line(l2: int, peak_gbs: float, frames: int, warmup: int):
     return out, wbytes, rot
 
 
+def microdecoder_extra(md: dict, sampler, cpu_seconds):
+    """The default run's microdecoder line: each mode's figures (from
+    microdecoder_line) with the clocks sampled while it ran, and the oracle's
+    frame on the host cores beside them (cpu_seconds None: no oracle)."""
+    line = {"workload": MICRODECODER, "desc": MICRODECODER_DESC, "metric": "effective int4 weight GB/s"}
+    for k, v in md.items():
+        line[k] = {kk: vv for kk, vv in v.items() if kk not in ("t0", "t1")}
+        line[k]["clocks"] = sampler.summary(v["t0"], v["t1"])
+    if cpu_seconds is not None:
+        cb, _, _ = time_oracle_microdecoder(cpu_seconds)
+        cb["cpu_model"] = cpu_model()
+        line["cpu_baseline"] = cb
+    return line
+
+
 def run_microdecoder(args, world, rank, local):
     import torch
     from w4a16_int4_quantized_gb300 import build, synth
@@ -1192,10 +1207,9 @@ def run_ours(args, world, rank, local):
         sampler.start()
         time.sleep(0.3)
         extra = extra_lines(l2, peaks, sampler, None if args.no_cpu else min(args.cpu_seconds, 1.0))
-        sampler.stop()
         md, _, _ = microdecoder_line(l2, float(peaks.get("hbm_gbs", HBM_FALLBACK_GBS)), 200, 3)
-        extra.append({"workload": MICRODECODER, "desc": MICRODECODER_DESC, "metric": "effective int4 weight GB/s",
-                      **{k: {kk: vv for kk, vv in v.items() if kk not in ("t0", "t1")} for k, v in md.items()}})
+        sampler.stop()
+        extra.append(microdecoder_extra(md, sampler, None if args.no_cpu else min(args.cpu_seconds, 1.0)))
     line = {
         "metric": metric_name(w),
         "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

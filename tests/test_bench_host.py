@@ -72,3 +72,31 @@ def test_reference_arm_bounded_for_many_steps():
 
 def test_cpu_model_is_named():
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_microdecoder_extra_line_has_clocks_and_oracle():
+    """The default run's microdecoder line: every mode keeps its figures and
+    gets the clocks sampled inside its own timed region; the oracle's frame
+    rate sits beside them."""
+    import datetime as dt
+    t0 = dt.datetime(2026, 1, 1, 12, 0, 0).timestamp()
+    sampler = bench.ClockSampler(None)
+    for i in range(20):  # one sample every 50 ms; a power-cap sample inside the second region
+        ts = dt.datetime.fromtimestamp(t0 + 0.05 * i).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        cap = "Active" if i == 12 else "Not Active"
+        sampler.lines.append(f"{ts}, {2070 - i}, 2070, 900.00, 0x0, Not Active, Not Active, Not Active, {cap}")
+    figures = {"ms_per_frame": 0.9, "frames_per_s": 1111.1, "weight_gbs": 570.0, "weight_sets": 9,
+               "frac_of_hbm": 0.084, "launches_per_frame": 1}
+    md = {"chain_rotating": {**figures, "t0": t0 + 0.02, "t1": t0 + 0.33},
+          "chain_l2_resident": {**figures, "t0": t0 + 0.52, "t1": t0 + 0.80}}
+    line = bench.microdecoder_extra(md, sampler, 0.05)
+    assert line["workload"] == bench.MICRODECODER
+    for k in md:
+        assert "t0" not in line[k] and line[k]["weight_gbs"] == 570.0
+    first, second = line["chain_rotating"]["clocks"], line["chain_l2_resident"]["clocks"]
+    assert first["samples"] == 6 and first["reasons"] == [] and first["sm_max_mhz"] == 2070
+    assert second["samples"] == 6 and second["reasons"] == ["sw_power_cap"]
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cpu_model"]
+    assert bench.microdecoder_extra(md, sampler, None).get("cpu_baseline") is None
+    json.dumps(line)
