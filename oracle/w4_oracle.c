@@ -21,6 +21,8 @@
  *    8 weight scale forgotten                    (s08)
  *    9 special summation order when M == 1       (s09)
  *   10 group that does not divide K accepted     (s10)
+ *   11 NULL weights not checked                 (s11: the read crashes; its
+ *      pin runs in a child process)
  *   12 last output row dropped when N % 8 != 0   (s12)
  *   13 +8 bias correction dropped
  *   14 ties rounded away from zero
@@ -46,8 +48,6 @@
  *   34 interleave reader swaps the two channels of a byte
  *   35 interleave reader drops the odd-K pad nibble
  *   36 W8A32 codes read as unsigned bytes
- * (s11, the missing NULL check, would crash the test process and is covered
- * by the host-side validation tests of the CUDA library instead.)
  */
 #pragma STDC FP_CONTRACT OFF
 
@@ -415,7 +415,11 @@ static int w4a16_check(const void *x, const void *w, const void *s, const void *
     if (G <= 0 || (G & 1) || (Kp % G) != 0) return REF_ESHAPE;
 #endif
     if (M == 0 || N == 0) return REF_OK;
+#if MUT(11)
+    if (!y || (K > 0 && (!x || !s))) return REF_EINVAL;
+#else
     if (!y || (K > 0 && (!x || !w || !s))) return REF_EINVAL;
+#endif
     return -1; /* proceed */
 }
 

@@ -393,6 +393,34 @@ def pin_shape_errors(o):
     assert st(0, 2, 4, 2) == REF_OK
 
 
+def pin_null_pointers(o):
+    """shape_and_argument_errors, NULL half ("Fused int4 ..." section 4: EINVAL
+    for NULL pointers, before any read, y untouched): each required pointer
+    missing in turn, with the others valid."""
+    import ctypes as C
+    M, N, K, G = 1, 2, 4, 2
+    x = np.zeros(M * K, np.uint16)
+    w = np.zeros(N * K // 2, np.uint8)
+    s = np.zeros(N * K // G, np.uint16)
+    y = np.full(M * N, 7.0, np.float32)
+    p = lambda a: a.ctypes.data_as(C.c_void_p)
+    args = [p(x), p(w), p(s), p(y)]
+    for i in range(4):
+        a = list(args)
+        a[i] = None
+        assert o.lib.ref_linear_w4a16_lanes(*a, M, N, K, G) == REF_EINVAL, i
+        assert np.all(y == 7.0)
+    assert o.lib.ref_linear_w4a16_lanes(*args, M, N, K, G) == REF_OK
+    xq, sx, sw = np.zeros(K, np.int8), np.ones(M, np.float32), np.ones(N, np.float32)
+    y[:] = 7.0
+    q4 = [p(xq), p(sx), p(w), p(sw), p(y)]
+    for i in range(5):
+        a = list(q4)
+        a[i] = None
+        assert o.lib.ref_linear_q4(*a, M, N, K) == REF_EINVAL, i
+        assert np.all(y == 7.0)
+
+
 # ---------------------------------------------------------------- inline-scale blocks of 32
 
 def pin_b32_closed_form(o):
