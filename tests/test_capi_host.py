@@ -246,3 +246,22 @@ def test_probe_and_version(lib):
     assert r.w4_probe_mma_peak(1, FAKE, 1 << 20, None, None) == lib.W4_EINVAL        # no result pointer
     ver = r.w4_version()
     assert ver >= 100 and ver // 10000 < 100
+
+
+def test_missing_library_fails_loudly(lib):
+    """No fallback: without the built library the binding refuses to load."""
+    with pytest.raises(RuntimeError, match="not built"):
+        lib.load(os.path.join(ROOT, "no_such_dir", "libw4gb300.so"))
+
+
+def test_product_never_touches_the_oracle():
+    """The package (binding, build script, generators) neither imports nor
+    names the oracle's module or library: the oracle is test infrastructure."""
+    pkg = os.path.join(ROOT, "w4a16_int4_quantized_gb300")
+    files = [os.path.join(pkg, f) for f in os.listdir(pkg) if f.endswith(".py")]
+    csrc = os.path.join(pkg, "csrc")
+    files += [os.path.join(csrc, f) for f in os.listdir(csrc)]
+    for path in files:
+        text = open(path, encoding="utf-8").read()
+        assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), path
+        assert "w4oracle" not in text and "w4_oracle" not in text, path
