@@ -100,3 +100,34 @@ def test_microdecoder_extra_line_has_clocks_and_oracle():
     assert cb["kind"] == "oracle" and cb["value"] > 0 and cb["cpu_model"]
     assert bench.microdecoder_extra(md, sampler, None).get("cpu_baseline") is None
     json.dumps(line)
+
+
+def test_measure_line_reports_cold_and_warm(monkeypatch):
+    """measure_line's host logic with the device parts faked: the cold figure
+    rotates input copies, the warm one runs every step on copy 0, and both
+    come from the same workload object."""
+    seen = []
+
+    class FakeWorkload:
+        launches_per_step = 1
+
+        def __init__(self, w, copies):
+            self.w, self.copies = w, copies
+
+    def fake_time_steps(wl, steps, warmup, kernel_only=False):
+        seen.append((wl.copies, kernel_only))
+        us = 2.0 if wl.copies == 1 else 4.0   # warm: weights already in L2
+        return steps * us / 1e3, 100.0, 100.1
+
+    monkeypatch.setattr(bench, "Workload", FakeWorkload)
+    monkeypatch.setattr(bench, "time_steps", fake_time_steps)
+    sampler = bench.ClockSampler(None)
+    name = "w4a16_decode_m1_n13312"
+    w = bench.WORKLOADS[name]
+    line = bench.measure_line(name, 128 << 20, {"hbm_gbs": 6759.9}, sampler, None)
+    copies = bench.copies_for(w, 128 << 20)
+    assert seen == [(copies, False), (copies, True), (1, False)]
+    assert line["us_per_step"] == 4.0 and line["warm_l2_resident"]["us_per_step"] == 2.0
+    assert line["warm_l2_resident"]["value"] == round(2 * line["value"], 2) or \
+        abs(line["warm_l2_resident"]["value"] - 2 * line["value"]) < 0.02
+    assert "cpu_baseline" not in line
